@@ -1,0 +1,161 @@
+/*
+ * nvfp4_moe.h -- C ABI of the NVFP4 sparse mixture-of-experts FFN layer (sm_103a).
+ *
+ * What the layer computes.  The Flint 40B-A2.5B pages ("Recursive Flint
+ * 40B-A2.5B：まず速さを第一に考えて作られたコーディングモデル", OrcaRouter blog,
+ * section "このアーキテクチャはメモリ帯域幅に関する主張である") give each MoE layer
+ * 256 routed experts, 6 of them chosen per token, plus one always-on shared
+ * expert, and ship the weights in NVFP4 (same page, section
+ * "量子化のレシピは最も転用しやすい部分です").  Everything else is a stated
+ * reading, identical in the library and its test oracle:
+ *
+ *   logits[t,e] = sum_k x[t,k] * W_r[k,e] (+ bias[e])            fp32
+ *   idx[t,:]    = the top_k largest logits, descending, ties -> lower e
+ *   w[t,j]      = softmax of the chosen logits (== full softmax renormalised)
+ *   expert_e(x) = W_down,e (silu(W_gate,e x) * W_up,e x)          SwiGLU, no bias
+ *   y[t]        = sum_j w[t,j] expert_{idx[t,j]}(x_t) + sum_s shared_s(x_t)
+ *
+ * NVFP4 tensor of R rows and K columns (K % 16 == 0), "canonical" layout:
+ *   codes  uint8 [R][K/2]   E2M1 codes, two per byte, even k in the low nibble
+ *   scales uint8 [R][K/16]  E4M3 (OCP E4M3FN) scale of each 16-element run along K
+ *   ts     fp32             one scale per tensor;  value = e2m1 * e4m3 * ts
+ * gate and up are [d_ff][d_model] (K = d_model), down is [d_model][d_ff].
+ * Arrays of several experts are stacked on the first index.
+ *
+ * Conventions for every call:
+ *   - Every pointer argument is a device pointer unless marked "host or
+ *     device"; activations are bf16 row-major [T][d_model].
+ *   - Argument errors are detected on the host before any work is queued and
+ *     returned as MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED; nothing is launched
+ *     then.  CUDA launch failures return MOE_ERR_CUDA.
+ *   - Forward calls are asynchronous on `stream` (NULL = legacy default
+ *     stream) and allocate nothing; all scratch is allocated by moe_init for
+ *     config.max_tokens.  Conditions found on the device are latched in a
+ *     device status word and reported by moe_get_device_status; no kernel
+ *     ever traps.
+ *   - A context is not thread-safe and its forward calls must not overlap on
+ *     the GPU (they share the context's scratch).
+ */
+#ifndef NVFP4_MOE_H
+#define NVFP4_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_ctx moe_ctx; /* opaque, owned by the library */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* NULL pointer, size out of range, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid but not implemented shape/format */
+  MOE_ERR_OOM = 3,           /* cudaMalloc failed in moe_init */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up */
+  MOE_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed */
+} moe_status;
+
+typedef enum { MOE_W_NVFP4 = 0, MOE_W_BF16 = 1 } moe_weight_format;
+
+typedef struct {
+  int d_model;        /* hidden size, multiple of 256, <= 8192                  */
+  int n_experts;      /* routed experts, 1..256                                  */
+  int top_k;          /* experts chosen per token, 1..min(8, n_experts)          */
+  int d_ff;           /* expert width, one of 64, 128, 256, 512, 1024            */
+  int n_shared;       /* always-on shared experts, 0..2                          */
+  int d_ff_shared;    /* width of the shared experts; must equal d_ff            */
+  int max_tokens;     /* largest T any forward call will pass, 1..65536          */
+  int weight_format;  /* moe_weight_format                                       */
+} moe_config;
+
+/* One weight matrix of a stack of experts (n = n_experts or n_shared).
+ * NVFP4: codes/scales/tensor_scale as described above, bf16 NULL.
+ * BF16:  bf16 = [n][rows][K] row-major bf16 values, the other three NULL.
+ * Pointers may be host or device; they are read during moe_init only. */
+typedef struct {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* tensor_scale;
+  const void* bf16;
+} moe_matrix;
+
+typedef struct {
+  const float* router;       /* [d_model][n_experts] fp32, host or device        */
+  const float* router_bias;  /* [n_experts] fp32 or NULL, host or device         */
+  moe_matrix gate, up, down; /* routed experts                                   */
+  moe_matrix shared_gate, shared_up, shared_down; /* shared experts (n_shared)   */
+} moe_weights;
+
+/* Validate the config, allocate the device arena on `device`, copy and
+ * repack the weights into the library's device layouts, allocate scratch for
+ * max_tokens.  On success *out owns all of it until moe_destroy. */
+MOE_API moe_status moe_init(const moe_config* cfg, const moe_weights* weights, int device,
+                    moe_ctx** out);
+
+/* Router only: logits, top-k, combine weights and per-expert token counts.
+ * x [T][d_model] bf16 -> idx [T][top_k] int32, w [T][top_k] fp32,
+ * counts [n_experts] int32 (any of the three outputs may be NULL).
+ * 0 <= T <= max_tokens. */
+MOE_API moe_status moe_route(moe_ctx* ctx, const void* x_bf16, int T, int32_t* idx, float* w,
+                     int32_t* counts, cudaStream_t stream);
+
+/* Decode form of the layer: activations stay exact (bf16 -> fp32), the NVFP4
+ * weights are dequantised on the fly.  y [T][d_model] bf16 (may not alias x).
+ * If `residual` is non-zero, y = bf16(x + layer(x)) (the stack's residual). */
+MOE_API moe_status moe_forward_decode(moe_ctx* ctx, const void* x_bf16, int T, void* y_bf16,
+                              int residual, cudaStream_t stream);
+
+/* Prefill form: x and the SwiGLU output h are quantised to NVFP4 (16-element
+ * E4M3 block scales, tensor scale 1) and every expert product runs as a
+ * block-scaled FP4 x FP4 tensor-core GEMM.  NVFP4 weights only. */
+MOE_API moe_status moe_forward_prefill(moe_ctx* ctx, const void* x_bf16, int T, void* y_bf16,
+                               int residual, cudaStream_t stream);
+
+/* Quantise n fp32 tensors w [n][rows][K] to canonical NVFP4 on the device:
+ * codes [n][rows][K/2], scales [n][rows][K/16], ts [n].  Rules (all fp32,
+ * round-to-nearest-even):  ts = amax/2688;  s = E4M3(amax_16 / (6*ts));
+ * q = E2M1(v / (e4m3(s)*ts)); zero tensors give ts = 0 and zero codes.
+ * K % 16 == 0.  Scratch-free; `w` is not modified. */
+MOE_API moe_status moe_quantize_nvfp4(const float* w, int n, int rows, int K, uint8_t* codes,
+                              uint8_t* scales, float* ts, cudaStream_t stream);
+
+/* Copy the quantised SwiGLU activations h of the last prefill call to the
+ * caller: h_codes [T*(top_k+n_shared)][d_ff/2], h_scales [...][d_ff/16], in
+ * slot order s = t*top_k + j for routed slots, T*top_k + i*T + t for shared
+ * expert i.  Asynchronous on `stream`.  For checking only. */
+MOE_API moe_status moe_debug_prefill_h(moe_ctx* ctx, int T, uint8_t* h_codes, uint8_t* h_scales,
+                               cudaStream_t stream);
+
+/* Record `start` / `stop` (cudaEvent_t, may be NULL to disable) around the
+ * expert kernels of every following forward call on its stream.  The records
+ * are external event records, so inside a stream capture they become event
+ * record nodes of the graph and can be timed after a replay. */
+MOE_API moe_status moe_set_profile_events(moe_ctx* ctx, cudaEvent_t start, cudaEvent_t stop);
+
+/* Synchronise the context's device and return the latched device status
+ * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK), then clear it. */
+MOE_API moe_status moe_get_device_status(moe_ctx* ctx);
+
+/* Number of kernels one forward call launches for T tokens (for accounting). */
+MOE_API int moe_kernels_per_forward(moe_ctx* ctx, int T, int prefill);
+
+/* Free everything the context owns.  NULL is accepted. */
+MOE_API moe_status moe_destroy(moe_ctx* ctx);
+
+/* Static description of a status code. */
+MOE_API const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_MOE_H */

@@ -1,0 +1,147 @@
+// Token -> expert bucketing: counts, exclusive offsets and a stable scatter.
+//
+// Not on the pages; it is the bookkeeping any batched MoE needs once the
+// router has chosen k experts per token.  Positions p order the (token,
+// expert) pairs by expert, token-major inside an expert; shared expert s
+// follows at T*k + s*T + t.  One block of 1024 threads:
+//   A. each warp takes chunks of 32 tokens; a per-warp bitmask per expert
+//      (atomicOr of 1 << lane) gives every pair its rank among the chunk's
+//      tokens that chose the same expert (popc of the lower lanes) and the
+//      chunk's count per expert;
+//   B. thread e turns its column of chunk counts into an exclusive prefix;
+//   C. warp 0 scans the per-expert totals into offsets and compacts the
+//      active experts (count > 0), shared experts appended;
+//   D. every pair lands at offsets[e] + prefix[chunk][e] + rank.
+// All sums are integer, so the result is exact and deterministic.
+#include "internal.h"
+
+namespace nvmoe {
+
+namespace {
+
+constexpr int kBucketThreads = 1024;
+constexpr int kMaxE = 256;
+
+__global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T, int k, int E,
+                                                                int S, int* status) {
+  __shared__ uint32_t mask[kBucketThreads / 32][kMaxE];
+  __shared__ int cnt[kMaxE];
+  __shared__ int off[kMaxE + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  const int nchunks = (T + 31) / 32;
+
+  // A. per-chunk ranks and counts
+  for (int c = warp; c < nchunks; c += nwarps) {
+    for (int e = lane; e < E; e += 32) mask[warp][e] = 0u;
+    __syncwarp();
+    const int t = c * 32 + lane;
+    const bool valid = t < T;
+    int ej[8];
+    if (valid) {
+      for (int j = 0; j < k; ++j) {
+        int e = r.idx[(size_t)t * k + j];
+        if (e < 0 || e >= E) { latch_status(status, MOE_ERR_DEVICE_CHECK); e = 0; }
+        ej[j] = e;
+        atomicOr(&mask[warp][e], 1u << lane);
+      }
+    }
+    __syncwarp();
+    if (valid) {
+      const uint32_t lower = (1u << lane) - 1u;
+      for (int j = 0; j < k; ++j) r.rank[(size_t)t * k + j] = __popc(mask[warp][ej[j]] & lower);
+    }
+    for (int e = lane; e < E; e += 32) r.chunk_cnt[(size_t)c * E + e] = __popc(mask[warp][e]);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // B. exclusive prefix of each expert's chunk counts
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    int run = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = r.chunk_cnt[(size_t)c * E + e];
+      r.chunk_cnt[(size_t)c * E + e] = run;
+      run += v;
+    }
+    cnt[e] = run;
+  }
+  __syncthreads();
+
+  // C. offsets and the active-expert list (warp 0, 8 experts per lane)
+  if (warp == 0) {
+    int local[8], lsum = 0, lact = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      local[i] = (e < E) ? cnt[e] : 0;
+      lsum += local[i];
+      lact += local[i] > 0;
+    }
+    int incl = lsum, aincl = lact;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      const int a = __shfl_up_sync(0xffffffffu, aincl, o);
+      if (lane >= o) { incl += v; aincl += a; }
+    }
+    int run = incl - lsum, a = aincl - lact;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      if (e < E) {
+        off[e] = run;
+        r.offsets[e] = run;
+        r.counts[e] = local[i];
+        if (local[i] > 0) {
+          r.act_e[a] = e;
+          r.act_pos[a] = run;
+          r.act_n[a] = local[i];
+          ++a;
+        }
+      }
+      run += local[i];
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int nact = __shfl_sync(0xffffffffu, aincl, 31);
+    if (lane == 0) {
+      off[E] = total;
+      r.offsets[E] = total;
+      int na = nact;
+      if (T > 0) {
+        for (int s = 0; s < S; ++s) {
+          r.act_e[na] = E + s;
+          r.act_pos[na] = T * k + s * T;
+          r.act_n[na] = T;
+          ++na;
+        }
+      }
+      *r.n_active = na;
+      if (total != T * k) latch_status(status, MOE_ERR_DEVICE_CHECK);
+    }
+  }
+  __syncthreads();
+
+  // D. stable scatter
+  for (int s = threadIdx.x; s < T * k; s += blockDim.x) {
+    const int t = s / k;
+    int e = r.idx[s];
+    if (e < 0 || e >= E) e = 0;
+    const int p = off[e] + r.chunk_cnt[(size_t)(t >> 5) * E + e] + r.rank[s];
+    r.perm[p] = s;
+    r.slot_pos[s] = p;
+    r.pos_tok[p] = t;
+  }
+  for (int q = threadIdx.x; q < S * T; q += blockDim.x) r.pos_tok[T * k + q] = q % T;
+}
+
+}  // namespace
+
+cudaError_t launch_bucket(const moe_ctx* c, int T, cudaStream_t s) {
+  bucket_kernel<<<1, kBucketThreads, 0, s>>>(c->r, T, c->cfg.top_k, c->cfg.n_experts,
+                                              c->cfg.n_shared, c->status);
+  return cudaGetLastError();
+}
+
+}  // namespace nvmoe

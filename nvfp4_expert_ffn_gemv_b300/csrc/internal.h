@@ -1,0 +1,57 @@
+// Host-side context and kernel launchers of the NVFP4 MoE library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+struct moe_ctx {
+  moe_config cfg;
+  int device = 0;
+  int n_all = 0;        // routed + shared experts
+  int sm_count = 0;
+
+  // one device arena holding every buffer below
+  uint8_t* arena = nullptr;
+  size_t arena_bytes = 0;
+
+  // weights (library layouts, see common.cuh)
+  uint8_t* gu_codes = nullptr;
+  uint8_t* gu_scales = nullptr;
+  uint8_t* dn_codes = nullptr;
+  uint8_t* dn_scales = nullptr;
+  float* tsc = nullptr;
+  __nv_bfloat16* gu_bf16 = nullptr;
+  __nv_bfloat16* dn_bf16 = nullptr;
+  float* router = nullptr;   // [d][E]
+  float* bias = nullptr;     // [E] (zeros when absent)
+  int has_bias = 0;
+
+  // scratch, sized for cfg.max_tokens
+  float* router_partial = nullptr;
+  nvmoe::Routing r{};
+  float* h = nullptr;        // [P][f] fp32, P = T*k + S*T positions
+  float* yexp = nullptr;     // [P][d] fp32 per-position expert outputs
+  int* status = nullptr;     // device status word
+  int max_positions = 0;
+
+  cudaEvent_t prof_start = nullptr;
+  cudaEvent_t prof_stop = nullptr;
+};
+
+namespace nvmoe {
+
+cudaError_t launch_router(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
+cudaError_t launch_bucket(const moe_ctx* c, int T, cudaStream_t s);
+cudaError_t launch_gateup_decode(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
+cudaError_t launch_down_decode(const moe_ctx* c, int T, cudaStream_t s);
+cudaError_t launch_combine(const moe_ctx* c, const __nv_bfloat16* x, int T, __nv_bfloat16* y,
+                           int residual, cudaStream_t s);
+cudaError_t launch_quantize_nvfp4(const float* w, int n, int rows, int K, uint8_t* codes,
+                                  uint8_t* scales, float* ts, cudaStream_t s);
+int router_chunks(int d, int T);
+cudaError_t prepare_decode_kernels(const moe_ctx* c);
+
+}  // namespace nvmoe
