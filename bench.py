@@ -140,7 +140,7 @@ def run_ours(args):
     s = synth.FLINT
     K, W = args.steps, args.warmup
     T = 64 if args.workload == "decode_b64" else 1
-    n_copies = 16
+    n_copies = int(os.environ.get("MOE_BENCH_COPIES", "16"))
     bias = synth.zipf_bias(s, seed=4242) if T == 64 else None
     ctxs = _build_layers(lib, torch, synth, n_copies, max_tokens=T, bias=bias, seed0=100 * rank)
     stream = torch.cuda.Stream()
@@ -182,20 +182,23 @@ def run_ours(args):
             torch.distributed.barrier()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        graph.replay()
-        b.record(stream)
+        with torch.cuda.stream(stream):          # replay() launches on the current stream
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         return a.elapsed_time(b)
 
-    for _ in range(2):
-        g.replay()                                # graph warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            g.replay()                            # graph warm-up
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         ms = timed(g)
-        gp.replay()
+        with torch.cuda.stream(stream):
+            gp.replay()
         torch.cuda.synchronize()
         kern_ms = sorted(a.elapsed_time(b) for a, b in ev)
     if world > 1:
@@ -214,7 +217,8 @@ def run_ours(args):
             xd.copy_(xh[i], non_blocking=True)
             lib.moe_forward_decode(ctxs[i % n_copies], xd, T, yd, 0, stream)
             yh[i].copy_(yd, non_blocking=True)
-    ge.replay()
+    with torch.cuda.stream(stream):
+        ge.replay()
     torch.cuda.synchronize()
     e2e_ms = timed(ge)
     if world > 1:

@@ -16,7 +16,8 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libnvfp4moe.so")
+#: the in-tree library; NVFP4_MOE_LIB may point at another build of the same ABI
+LIB_PATH = os.environ.get("NVFP4_MOE_LIB") or os.path.join(_HERE, "libnvfp4moe.so")
 
 MOE_OK = 0
 MOE_W_NVFP4 = 0

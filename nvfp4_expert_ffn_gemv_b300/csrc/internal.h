@@ -37,6 +37,15 @@ struct moe_ctx {
   int* status = nullptr;     // device status word
   int max_positions = 0;
 
+  // batch-1 decode fast path (see decode_b1.cu / repack.cu)
+  int b1_enabled = 0;
+  int b1_grid = 0, b1_rmax = 0, b1_nbmax = 0;
+  size_t b1_smem = 0;
+  float* router_t = nullptr;     // [E][d]
+  uint8_t* b1_rows = nullptr;    // [n_all][f][1.125 d] gate/up records per hidden row
+  float* logits = nullptr;       // [E]
+  unsigned* ticket = nullptr;    // CTA completion counters, zero between calls
+
   cudaEvent_t prof_start = nullptr;
   cudaEvent_t prof_stop = nullptr;
 };
@@ -53,5 +62,13 @@ cudaError_t launch_quantize_nvfp4(const float* w, int n, int rows, int K, uint8_
                                   uint8_t* scales, float* ts, cudaStream_t s);
 int router_chunks(int d, int T);
 cudaError_t prepare_decode_kernels(const moe_ctx* c);
+bool b1_supported(const moe_config& c);
+bool b1_plan(const moe_config& c, int sm_count, int ctas_per_sm, int* grid, int* rmax, int* nbmax, size_t* smem);
+size_t b1_row_bytes(int d);
+cudaError_t prepare_b1_kernels(const moe_ctx* c);
+cudaError_t repack_b1_layouts(moe_ctx* c);
+cudaError_t launch_router_b1(const moe_ctx* c, const __nv_bfloat16* x, cudaStream_t s);
+cudaError_t launch_experts_b1(const moe_ctx* c, const __nv_bfloat16* x, __nv_bfloat16* y, int residual,
+                              cudaStream_t s);
 
 }  // namespace nvmoe

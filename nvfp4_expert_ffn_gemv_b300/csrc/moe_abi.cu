@@ -1,6 +1,7 @@
 // C ABI of the NVFP4 MoE library: argument checks, device arena, weight
 // repacking and the per-call kernel sequence.  See include/nvfp4_moe.h.
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -76,6 +77,12 @@ size_t carve(moe_ctx* x, uint8_t* base) {
   x->h = cv.take<float>(base, P * f);
   x->yexp = cv.take<float>(base, P * d);
   x->status = cv.take<int>(base, 1);
+  if (x->b1_enabled) {
+    x->router_t = cv.take<float>(base, d * E);
+    x->b1_rows = cv.take<uint8_t>(base, n * f * b1_row_bytes((int)d));
+    x->logits = cv.take<float>(base, E);
+    x->ticket = cv.take<unsigned>(base, 4);
+  }
   x->max_positions = (int)P;
   return cv.off;
 }
@@ -160,6 +167,12 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
   x->device = device;
   x->n_all = c.n_experts + c.n_shared;
   cudaDeviceGetAttribute(&x->sm_count, cudaDevAttrMultiProcessorCount, device);
+  if (b1_supported(c)) {
+    const char* env = getenv("NVFP4_MOE_B1_CTAS_PER_SM");
+    const int per_sm = env ? atoi(env) : 1;
+    x->b1_enabled = b1_plan(c, x->sm_count, per_sm > 0 ? per_sm : 1, &x->b1_grid, &x->b1_rmax, &x->b1_nbmax,
+                            &x->b1_smem);
+  }
   x->arena_bytes = carve(x, nullptr);
   if (cudaMalloc(&x->arena, x->arena_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -229,6 +242,11 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
   }
   if (e == cudaSuccess) e = cudaMemset(x->status, 0, sizeof(int));
   if (e == cudaSuccess) e = prepare_decode_kernels(x);
+  if (e == cudaSuccess && x->b1_enabled) {
+    e = repack_b1_layouts(x);
+    if (e == cudaSuccess) e = cudaMemset(x->ticket, 0, sizeof(unsigned) * 4);
+    if (e == cudaSuccess) e = prepare_b1_kernels(x);
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail(e);
   *out = x;
@@ -278,6 +296,13 @@ moe_status moe_forward_decode(moe_ctx* x, const void* x_bf16, int T, void* y_bf1
   if (T == 0) return MOE_OK;
   ensure_device(x->device);
   const auto* xb = static_cast<const __nv_bfloat16*>(x_bf16);
+  if (T == 1 && x->b1_enabled) {
+    CK(launch_router_b1(x, xb, s));
+    if (x->prof_start) CK(cudaEventRecordWithFlags(x->prof_start, s, cudaEventRecordExternal));
+    CK(launch_experts_b1(x, xb, static_cast<__nv_bfloat16*>(y_bf16), residual, s));
+    if (x->prof_stop) CK(cudaEventRecordWithFlags(x->prof_stop, s, cudaEventRecordExternal));
+    return MOE_OK;
+  }
   CK(launch_router(x, xb, T, s));
   CK(launch_bucket(x, T, s));
   if (x->prof_start) CK(cudaEventRecordWithFlags(x->prof_start, s, cudaEventRecordExternal));
@@ -333,7 +358,7 @@ moe_status moe_get_device_status(moe_ctx* x) {
 
 int moe_kernels_per_forward(moe_ctx* x, int T, int prefill) {
   if (!x || T <= 0) return 0;
-  (void)prefill;
+  if (!prefill && T == 1 && x->b1_enabled) return 3;
   return 6;
 }
 

@@ -76,12 +76,27 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
     taken[i] = e >= E;
-    float s = 0.f;
-    if (e < E) {
-      for (int kc = 0; kc < nkc; ++kc) s += part[((size_t)kc * T + t) * E + e];
-      if (has_bias) s += bias[e];
+    v[i] = 0.f;
+  }
+  // partial sums in a fixed order; 8 independent loads in flight per step
+  for (int kc0 = 0; kc0 < nkc; kc0 += 8) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        float pv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          pv[q] = (kc0 + q < nkc) ? __ldg(part + ((size_t)(kc0 + q) * T + t) * E + e) : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[i] += pv[q];
+      }
     }
-    v[i] = s;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && has_bias) v[i] += bias[e];
   }
   float sel_v[8];
   int sel_e[8];
