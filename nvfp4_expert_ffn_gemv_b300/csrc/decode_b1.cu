@@ -198,7 +198,6 @@ __global__ void __launch_bounds__(64) router_b1_kernel(const float* __restrict__
   }
   if (l == 0) *ticket = 0u;
 }
-}
 
 // ---------------------------------------------------------------------------
 // experts
