@@ -129,6 +129,8 @@ struct Routing {
   int32_t* act_pos;    // [E+S] first position of each active expert
   int32_t* act_n;      // [E+S] tokens of each active expert
   int32_t* n_active;   // [1]
+  int32_t* act_ppos;   // [E+S+1] prefill: padded first row (multiple of 128), total last
+  int32_t* act_ntb;    // [E+S+1] prefill: first 256-token N tile, total last
   int32_t* chunk_cnt;  // [ceil(T/32)][E] scratch
   int32_t* rank;       // [T*k] scratch
 };

@@ -1,6 +1,7 @@
 // Host-side context and kernel launchers of the NVFP4 MoE library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -46,6 +47,17 @@ struct moe_ctx {
   float* logits = nullptr;       // [E]
   unsigned* ticket = nullptr;    // CTA completion counters, zero between calls
 
+  // prefill (see prefill.cu)
+  int pf_enabled = 0;
+  int last_prefill_T = -1;
+  uint8_t* pf_sfa_gu = nullptr;  // gate/up weight scale atoms [n_all][2f/128][d/64][512]
+  uint8_t* pf_sfa_dn = nullptr;  // W_down scale atoms [n_all][d/128][f/64][512]
+  uint8_t* pf_xq = nullptr;      // x in NVFP4, padded positions [rows][d/2]
+  uint8_t* pf_xsf = nullptr;     // its scale atoms [rows/128][d/64][512]
+  uint8_t* pf_hq = nullptr;      // h in NVFP4 [rows][f/2]
+  uint8_t* pf_hsf = nullptr;     // its scale atoms [rows/128][f/64][512]
+  CUtensorMap pf_tm[4];          // gate/up codes, W_down codes, x codes, h codes
+
   cudaEvent_t prof_start = nullptr;
   cudaEvent_t prof_stop = nullptr;
 };
@@ -62,6 +74,11 @@ cudaError_t launch_quantize_nvfp4(const float* w, int n, int rows, int K, uint8_
                                   uint8_t* scales, float* ts, cudaStream_t s);
 int router_chunks(int d, int T);
 cudaError_t prepare_decode_kernels(const moe_ctx* c);
+bool prefill_supported(const moe_config& c);
+size_t prefill_max_rows(const moe_config& c);
+cudaError_t prefill_prepare(moe_ctx* c);
+cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
+cudaError_t launch_gather_prefill_h(const moe_ctx* c, int T, uint8_t* codes, uint8_t* sf, cudaStream_t s);
 bool b1_supported(const moe_config& c);
 bool b1_plan(const moe_config& c, int sm_count, int ctas_per_sm, int* grid, int* rmax, int* nbmax, size_t* smem);
 size_t b1_row_bytes(int d);

@@ -72,6 +72,8 @@ size_t carve(moe_ctx* x, uint8_t* base) {
   x->r.act_pos = cv.take<int32_t>(base, E + S);
   x->r.act_n = cv.take<int32_t>(base, E + S);
   x->r.n_active = cv.take<int32_t>(base, 1);
+  x->r.act_ppos = cv.take<int32_t>(base, E + S + 1);
+  x->r.act_ntb = cv.take<int32_t>(base, E + S + 1);
   x->r.chunk_cnt = cv.take<int32_t>(base, ((T + 31) / 32) * E);
   x->r.rank = cv.take<int32_t>(base, T * k);
   x->h = cv.take<float>(base, P * f);
@@ -84,6 +86,15 @@ size_t carve(moe_ctx* x, uint8_t* base) {
     x->ticket = cv.take<unsigned>(base, 4);
   }
   x->max_positions = (int)P;
+  if (x->pf_enabled) {
+    const size_t rows = prefill_max_rows(c);
+    x->pf_sfa_gu = cv.take<uint8_t>(base, n * 2 * f * d / 16);
+    x->pf_sfa_dn = cv.take<uint8_t>(base, n * d * f / 16);
+    x->pf_xq = cv.take<uint8_t>(base, rows * d / 2);
+    x->pf_xsf = cv.take<uint8_t>(base, rows * d / 16);
+    x->pf_hq = cv.take<uint8_t>(base, rows * f / 2);
+    x->pf_hsf = cv.take<uint8_t>(base, rows * f / 16);
+  }
   return cv.off;
 }
 
@@ -173,6 +184,7 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
     x->b1_enabled = b1_plan(c, x->sm_count, per_sm > 0 ? per_sm : 1, &x->b1_grid, &x->b1_rmax, &x->b1_nbmax,
                             &x->b1_smem);
   }
+  x->pf_enabled = prefill_supported(c);
   x->arena_bytes = carve(x, nullptr);
   if (cudaMalloc(&x->arena, x->arena_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -242,6 +254,11 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
   }
   if (e == cudaSuccess) e = cudaMemset(x->status, 0, sizeof(int));
   if (e == cudaSuccess) e = prepare_decode_kernels(x);
+  if (e == cudaSuccess && x->pf_enabled) {
+    e = prefill_prepare(x);
+    if (e == cudaSuccess) e = cudaMemset(x->pf_hq, 0, prefill_max_rows(c) * (f / 2));
+    if (e == cudaSuccess) e = cudaMemset(x->pf_hsf, 0, prefill_max_rows(c) * (f / 16));
+  }
   if (e == cudaSuccess && x->b1_enabled) {
     e = repack_b1_layouts(x);
     if (e == cudaSuccess) e = cudaMemset(x->ticket, 0, sizeof(unsigned) * 4);
@@ -317,16 +334,29 @@ moe_status moe_forward_prefill(moe_ctx* x, const void* x_bf16, int T, void* y_bf
                                cudaStream_t s) {
   moe_status st = check_fwd(x, x_bf16, T, y_bf16);
   if (st != MOE_OK) return st;
-  (void)residual;
-  (void)s;
-  return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && !y_bf16) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && x_bf16 == y_bf16) return MOE_ERR_INVALID_ARG;
+  if (!x->pf_enabled) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  ensure_device(x->device);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x_bf16);
+  CK(launch_router(x, xb, T, s));
+  CK(launch_bucket(x, T, s));
+  if (x->prof_start) CK(cudaEventRecordWithFlags(x->prof_start, s, cudaEventRecordExternal));
+  CK(launch_prefill_experts(x, xb, T, s));
+  if (x->prof_stop) CK(cudaEventRecordWithFlags(x->prof_stop, s, cudaEventRecordExternal));
+  CK(launch_combine(x, xb, T, static_cast<__nv_bfloat16*>(y_bf16), residual, s));
+  x->last_prefill_T = T;
+  return MOE_OK;
 }
 
-moe_status moe_debug_prefill_h(moe_ctx* x, int T, uint8_t* h_codes, uint8_t* h_scales,
-                               cudaStream_t s) {
+moe_status moe_debug_prefill_h(moe_ctx* x, int T, uint8_t* h_codes, uint8_t* h_scales, cudaStream_t s) {
   if (!x || !h_codes || !h_scales || T < 0 || T > x->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
-  (void)s;
-  return MOE_ERR_UNSUPPORTED;
+  if (!x->pf_enabled) return MOE_ERR_UNSUPPORTED;
+  if (T != x->last_prefill_T) return MOE_ERR_INVALID_ARG;
+  ensure_device(x->device);
+  CK(launch_gather_prefill_h(x, T, h_codes, h_scales, s));
+  return MOE_OK;
 }
 
 moe_status moe_quantize_nvfp4(const float* w, int n, int rows, int K, uint8_t* codes, uint8_t* scales,
@@ -359,6 +389,7 @@ moe_status moe_get_device_status(moe_ctx* x) {
 int moe_kernels_per_forward(moe_ctx* x, int T, int prefill) {
   if (!x || T <= 0) return 0;
   if (!prefill && T == 1 && x->b1_enabled) return 3;
+  if (prefill) return 8;   // router x2, bucket, plan, quantise x, GEMM x2, combine
   return 6;
 }
 

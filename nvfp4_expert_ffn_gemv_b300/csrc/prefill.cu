@@ -1,0 +1,535 @@
+// Prefill: block-scaled FP4 x FP4 grouped GEMMs on the 5th-generation tensor
+// cores (tcgen05.mma kind::mxf4nvf4, scales in tensor memory).
+//
+// The pages list prompt-processing kernels among the vendor's custom kernels
+// ("Recursive Flint 40B-A2.5B：まず速さを第一に考えて作られたコーディングモデル",
+// section "量子化のレシピは最も転用しやすい部分です") without describing them.
+// Here prefill is the one place where the MoE layer is a dense contraction
+// (~96 tokens per routed expert at 4096 tokens, all tokens for the shared
+// expert), so it runs on the tensor cores with both operands in NVFP4:
+//
+//   1. plan:   padded position blocks per active expert (multiples of 128
+//              tokens) and the prefix of 256-token N tiles;
+//   2. x -> NVFP4 (16-element E4M3 block scales, tensor scale 1) gathered into
+//              the padded blocks, scales written straight into the
+//              scale-factor atoms the MMA reads;
+//   3. GEMM gate/up, swap-AB: D[128 weight rows, N tokens] per (expert,
+//              128-row tile, N tile); the 128-row tile of the gate/up layout
+//              holds 64 gate rows and the matching 64 up rows, so the epilogue
+//              forms h = silu(g) * u for 64 hidden units and quantises it
+//              to NVFP4 (again block 16, scale 1) into the second GEMM's
+//              operand layout;
+//   4. GEMM down: D[128 output dims, N tokens] * ts_down -> per-slot rows of
+//              yexp (fp32), then the decode path's fixed-order combine.
+//
+// GEMM kernel: persistent, one CTA (192 threads) per SM, 512 TMEM columns.
+//   warp 0  TMA producer: 3-stage ring of {A 128x256 fp4 (SW128), B <=256x256
+//           fp4 (SW128, 32-row boxes), SFA 4 atoms, SFB 4-8 atoms}
+//   warp 1  TMEM owner + single-thread MMA issuer: per stage, scale atoms ->
+//           TMEM (tcgen05.cp 32x128b.warpx4), 4 MMAs of K = 64
+//   warps 2-5 epilogue (TMEM lanes 32*(warp%4) ..), tcgen05.ld 32 columns
+// All waits are bounded; the first one that gives up latches MOE_ERR_TIMEOUT
+// and sets a CTA-wide abort flag so that no other role waits afterwards.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace nvmoe {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kBM = 128;        // weight rows per tile
+constexpr int kStageK = 256;    // fp4 elements of K per stage (128 bytes per row)
+constexpr int kStages = 3;
+constexpr int kMaxN = 256;      // tokens per N tile
+constexpr int kBoxN = 32;       // rows per TMA box of the activation operand
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSfCol0 = 256;    // scale-factor columns start after D
+constexpr int kSfColsPerStage = 48;  // SFA 4 k-steps x 4 + SFB 4 k-steps x 8
+
+// shared-memory plan of the GEMM kernel (offsets from a 1024-aligned base)
+constexpr int kA = kBM * 128;                 // 16 KB per stage
+constexpr int kB = kMaxN * 128;               // 32 KB per stage
+constexpr int kSFA = 4 * 512;                 // 2 KB
+constexpr int kSFB = 2 * 4 * 512;             // 4 KB
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kA;
+constexpr int kOffSFA = kOffB + kStages * kB;
+constexpr int kOffSFB = kOffSFA + kStages * kSFA;
+constexpr int kOffU = kOffSFB + kStages * kSFB;     // 64 x 32 fp32 exchange buffer
+constexpr int kSmemGemm = kOffU + 64 * 32 * 4 + 1024;  // + alignment slack
+
+// ---------------------------------------------------------------------------
+// plan: padded positions and N-tile prefix per active expert (one warp)
+// ---------------------------------------------------------------------------
+__global__ void prefill_plan_kernel(Routing r) {
+  const int lane = threadIdx.x;
+  const int na = *r.n_active;
+  int pp = 0, nt = 0;
+  for (int base = 0; base < na; base += 32) {
+    const int a = base + lane;
+    const int n = a < na ? r.act_n[a] : 0;
+    int vp = (n + 127) / 128 * 128, vt = (n + kMaxN - 1) / kMaxN;
+    int ip = vp, it = vt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int up = __shfl_up_sync(0xffffffffu, ip, o), ut = __shfl_up_sync(0xffffffffu, it, o);
+      if (lane >= o) { ip += up; it += ut; }
+    }
+    if (a < na) {
+      r.act_ppos[a] = pp + ip - vp;
+      r.act_ntb[a] = nt + it - vt;
+    }
+    pp += __shfl_sync(0xffffffffu, ip, 31);
+    nt += __shfl_sync(0xffffffffu, it, 31);
+  }
+  if (lane == 0) {
+    r.act_ppos[na] = pp;
+    r.act_ntb[na] = nt;
+  }
+}
+
+// largest a < na with tab[a] <= v (tab non-decreasing, tab[0] = 0)
+__device__ __forceinline__ int find_seg(const int32_t* tab, int na, int v) {
+  int lo = 0, hi = na - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(tab + mid) <= v) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 block quantisation with tensor scale 1 (same rules as the weights)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t q_e4m3(float v) {
+  uint16_t out;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(0.0f), "f"(v));
+  return out & 0xFF;
+}
+__device__ __forceinline__ uint32_t q_e2m1x2(float even, float odd) {
+  uint16_t out;
+  asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n\tcvt.u16.u8 %0, b;\n\t}"
+      : "=h"(out) : "f"(odd), "f"(even));
+  uint32_t v = out & 0xFF;
+  if ((v & 0x07) == 0) v &= 0xF0;
+  if ((v & 0x70) == 0) v &= 0x0F;
+  return v;
+}
+
+// byte offset of the scale of (row p, 16-block b) in a [rows/128][ksteps][512] atom array
+__device__ __forceinline__ size_t sf_atom_offset(int p, int b, int ksteps) {
+  return ((size_t)(p >> 7) * ksteps + (b >> 2)) * 512 + (p & 31) * 16 + ((p >> 5) & 3) * 4 + (b & 3);
+}
+
+// x rows -> NVFP4 in padded position order; one warp per padded row, each lane
+// four 16-element blocks (d = 2048) or fewer.
+__global__ void __launch_bounds__(256) quant_x_kernel(Routing r, const __nv_bfloat16* __restrict__ x, int d,
+                                                      uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                      int max_rows) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p = blockIdx.x * 8 + warp;
+  const int na = *r.n_active;
+  const int total = r.act_ppos[na];
+  if (p >= total || p >= max_rows) return;
+  const int a = find_seg(r.act_ppos, na, p);
+  const int i = p - r.act_ppos[a];
+  const bool real = i < r.act_n[a];
+  const int t = real ? r.pos_tok[r.act_pos[a] + i] : 0;
+  const int nblk = d / 16, ksteps = d / 64;
+  for (int b = lane; b < nblk; b += 32) {
+    float v[16];
+    if (real) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + b * 16);
+      const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+      const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v[2 * q] = __uint_as_float(w[q] << 16);
+        v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) v[q] = 0.f;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+    const uint32_t s = q_e4m3(__fdiv_rn(amax, 6.0f));
+    const float dq = e4m3_to_f32(s);
+    uint32_t lo = 0, hi = 0;
+    if (dq > 0.f) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        lo |= q_e2m1x2(__fdiv_rn(v[2 * q], dq), __fdiv_rn(v[2 * q + 1], dq)) << (8 * q);
+        hi |= q_e2m1x2(__fdiv_rn(v[8 + 2 * q], dq), __fdiv_rn(v[8 + 2 * q + 1], dq)) << (8 * q);
+      }
+    }
+    reinterpret_cast<uint2*>(codes + (size_t)p * (d / 2))[b] = make_uint2(lo, hi);
+    sf[sf_atom_offset(p, b, ksteps)] = static_cast<uint8_t>(s);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the grouped GEMM
+// ---------------------------------------------------------------------------
+struct GemmArgs {
+  Routing r;
+  const uint8_t* sfa;     // weight scale atoms [n_all][mtiles][ksteps][512]
+  const uint8_t* sfb;     // activation scale atoms [rows/128][ksteps][512]
+  const float* tsc;       // [n_all][3]
+  int M;                  // weight rows per expert (2f or d)
+  int K;                  // contraction length
+  int mode;               // 0: gate/up -> h (NVFP4), 1: down -> yexp
+  // mode 0 outputs
+  uint8_t* hq_codes;      // [rows][f/2]
+  uint8_t* hq_sf;         // [rows/128][f/64][512]
+  int f;
+  // mode 1 output
+  float* yexp;            // [positions][d]
+  int d;
+  int* status;
+};
+
+struct UnitInfo {
+  int a, e, n0, N, nmma, mt, pos0, nbox, natoms;
+};
+
+__device__ __forceinline__ UnitInfo decode_unit(const GemmArgs& g, int u, int mtiles, int na) {
+  UnitInfo ui;
+  const int ntg = u / mtiles;
+  ui.mt = u % mtiles;
+  ui.a = find_seg(g.r.act_ntb, na, ntg);
+  const int nt = ntg - g.r.act_ntb[ui.a];
+  ui.e = g.r.act_e[ui.a];
+  const int n = g.r.act_n[ui.a];
+  ui.n0 = g.r.act_ppos[ui.a] + nt * kMaxN;
+  ui.N = min(kMaxN, n - nt * kMaxN);
+  ui.nmma = (ui.N + 15) / 16 * 16;
+  ui.pos0 = g.r.act_pos[ui.a] + nt * kMaxN;
+  ui.nbox = (ui.N + kBoxN - 1) / kBoxN;
+  ui.natoms = (ui.N + 127) / 128;
+  return ui;
+}
+
+__device__ __forceinline__ float silu_acc(float z) { return z / (1.0f + expf(-z)); }
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], dfull_bar, dempty_bar;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int na = *g.r.n_active;
+  const int mtiles = g.M / kBM, ksteps = g.K / 64, kstages = g.K / kStageK;
+  const int U = g.r.act_ntb[na] * mtiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&dfull_bar, 1);
+    mbar_init(&dempty_bar, 4);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) tmem_alloc(&tmem_base_s, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  auto bounded_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (abort_flag) return false;
+    if (wait_parity(bar, parity)) return true;
+    abort_flag = 1;
+    latch_status(g.status, MOE_ERR_TIMEOUT);
+    return false;
+  };
+
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
+        const UnitInfo ui = decode_unit(g, u, mtiles, na);
+        const int arow = ui.e * g.M + ui.mt * kBM;
+        for (int ks = 0; ks < kstages; ++ks) {
+          if (!bounded_wait(&empty_bar[stage], phase ^ 1)) break;
+          const uint32_t bytes = kA + ui.nbox * kBoxN * 128 + kSFA + ui.natoms * 4 * 512;
+          mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          tma_load_2d(smem + kOffA + stage * kA, &tmA, ks * 128, arow, &full_bar[stage]);
+          for (int b = 0; b < ui.nbox; ++b)
+            tma_load_2d(smem + kOffB + stage * kB + b * kBoxN * 128, &tmB, ks * 128, ui.n0 + b * kBoxN,
+                        &full_bar[stage]);
+          bulk_load(smem + kOffSFA + stage * kSFA,
+                    g.sfa + (((size_t)ui.e * mtiles + ui.mt) * ksteps + ks * 4) * 512, kSFA, &full_bar[stage]);
+          for (int at = 0; at < ui.natoms; ++at)
+            bulk_load(smem + kOffSFB + stage * kSFB + at * 2048,
+                      g.sfb + (((size_t)(ui.n0 >> 7) + at) * ksteps + ks * 4) * 512, 2048, &full_bar[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ----------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, dphase = 0;
+      for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
+        const UnitInfo ui = decode_unit(g, u, mtiles, na);
+        if (!bounded_wait(&dempty_bar, dphase ^ 1)) break;
+        dphase ^= 1;
+        tc_fence_after();
+        const uint32_t idesc = idesc_mxf4nvf4(kBM, ui.nmma);
+        for (int ks = 0; ks < kstages; ++ks) {
+          if (!bounded_wait(&full_bar[stage], phase)) break;
+          tc_fence_after();
+          const uint32_t sf = tmem + kSfCol0 + stage * kSfColsPerStage;
+          const uint32_t sa = smem_u32(smem + kOffSFA + stage * kSFA);
+          const uint32_t sb = smem_u32(smem + kOffSFB + stage * kSFB);
+          for (int kk = 0; kk < 4; ++kk) {
+            tmem_cp_sf_atom(sf + kk * 4, desc_sf_atom(sa + kk * 512));
+            for (int at = 0; at < ui.natoms; ++at)
+              tmem_cp_sf_atom(sf + 16 + kk * 8 + at * 4, desc_sf_atom(sb + at * 2048 + kk * 512));
+          }
+          const uint64_t adesc = desc_kmajor_sw128(smem_u32(smem + kOffA + stage * kA));
+          const uint64_t bdesc = desc_kmajor_sw128(smem_u32(smem + kOffB + stage * kB));
+          for (int kk = 0; kk < 4; ++kk)
+            mma_mxf4nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, sf + kk * 4,
+                         sf + 16 + kk * 8, ks > 0 || kk > 0);
+          tc_commit(&empty_bar[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        tc_commit(&dfull_bar);
+      }
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;              // TMEM lane quadrant
+    const int m = q * 32 + lane;         // tile row held by this thread
+    float* ubuf = reinterpret_cast<float*>(smem + kOffU);
+    uint32_t dphase = 0;
+    // Every epilogue warp runs the same units and column chunks and never leaves
+    // the loop early (a failed wait only skips the work), so the named-barrier
+    // counts of the four warps always match.
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+      const UnitInfo ui = decode_unit(g, u, mtiles, na);
+      const bool ok = bounded_wait(&dfull_bar, dphase);
+      dphase ^= 1;
+      tc_fence_after();
+      const float* ts = g.tsc + ui.e * 3;
+      for (int c0 = 0; c0 < ui.nmma; c0 += 32) {
+        uint32_t v[32];
+        if (ok) {
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
+        }
+        if (g.mode == 0) {
+          // rows 0..63 gate, 64..127 up (same hidden units); quadrants 2,3 hand their up values over
+          if (q >= 2) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ubuf[(m - 64) * 32 + j] = __uint_as_float(v[j]);
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (q < 2) {
+            const int jh = ui.mt * 64 + m;      // hidden unit
+            const int b = jh >> 4;              // its 16-block along d_ff
+            const int fsteps = g.f / 64;
+#pragma unroll 4
+            for (int j = 0; j < 32; ++j) {
+              const float gg = __uint_as_float(v[j]) * ts[0];
+              const float uu = ubuf[m * 32 + j] * ts[1];
+              const float h = silu_acc(gg) * uu;
+              // block amax over the 16 lanes that hold this token's 16 hidden units
+              float am = fabsf(h);
+#pragma unroll
+              for (int o = 1; o < 16; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+              const uint32_t s = q_e4m3(__fdiv_rn(am, 6.0f));
+              const float dq = e4m3_to_f32(s);
+              const float hn = dq > 0.f ? __fdiv_rn(h, dq) : 0.f;
+              const float partner = __shfl_xor_sync(0xffffffffu, hn, 1);
+              const int p = ui.n0 + c0 + j;     // padded row of this token
+              if (ok && (lane & 1) == 0) {
+                const uint32_t byte = dq > 0.f ? q_e2m1x2(hn, partner) : 0u;
+                g.hq_codes[(size_t)p * (g.f / 2) + (jh >> 1)] = static_cast<uint8_t>(byte);
+              }
+              if (ok && (lane & 15) == 0) g.hq_sf[sf_atom_offset(p, b, fsteps)] = static_cast<uint8_t>(s);
+            }
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+        } else {
+          const int rdim = ui.mt * kBM + m;
+#pragma unroll 8
+          for (int j = 0; j < 32; ++j) {
+            if (ok && c0 + j < ui.N)
+              g.yexp[(size_t)(ui.pos0 + c0 + j) * g.d + rdim] = __uint_as_float(v[j]) * ts[2];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(&dempty_bar);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows][row_bytes], boxes of box_rows x 128 bytes, 128-byte swizzle
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// weight scales [n][M][K/16] -> atoms [n][M/128][K/64][512]; one thread per output byte
+__global__ void weight_sf_atoms_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, size_t n, int M,
+                                       int K) {
+  const size_t total = n * (size_t)M * (K / 16);
+  const size_t o = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (o >= total) return;
+  const int ksteps = K / 64, mtiles = M / 128;
+  const size_t atom = o / 512;
+  const int w = (int)(o % 512);
+  const int ks = (int)(atom % ksteps);
+  const size_t rest = atom / ksteps;
+  const int mt = (int)(rest % mtiles);
+  const size_t e = rest / mtiles;
+  const int lr = w / 16, col = (w % 16) / 4, kb = w % 4;
+  const int row = mt * 128 + col * 32 + lr;
+  dst[o] = src[(e * M + row) * (K / 16) + ks * 4 + kb];
+}
+
+}  // namespace
+
+bool prefill_supported(const moe_config& c) {
+  return c.weight_format == MOE_W_NVFP4 && c.d_model % 256 == 0 && c.d_ff % 256 == 0 && c.d_model <= 8192;
+}
+
+size_t prefill_max_rows(const moe_config& c) {
+  const size_t T = c.max_tokens, k = c.top_k, S = c.n_shared, E = c.n_experts;
+  return (T * (k + S) + 128 * (E + S) + 127) / 128 * 128;
+}
+
+cudaError_t prefill_prepare(moe_ctx* c) {
+  const int d = c->cfg.d_model, f = c->cfg.d_ff, n = c->n_all;
+  const size_t t1 = (size_t)n * 2 * f * (d / 16), t2 = (size_t)n * d * (f / 16);
+  weight_sf_atoms_kernel<<<(unsigned)((t1 + 255) / 256), 256>>>(c->gu_scales, c->pf_sfa_gu, n, 2 * f, d);
+  weight_sf_atoms_kernel<<<(unsigned)((t2 + 255) / 256), 256>>>(c->dn_scales, c->pf_sfa_dn, n, d, f);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t rows = prefill_max_rows(c->cfg);
+  bool ok = make_tmap(&c->pf_tm[0], c->gu_codes, (uint64_t)n * 2 * f, d / 2, kBM) &&
+            make_tmap(&c->pf_tm[1], c->dn_codes, (uint64_t)n * d, f / 2, kBM) &&
+            make_tmap(&c->pf_tm[2], c->pf_xq, rows, d / 2, kBoxN) &&
+            make_tmap(&c->pf_tm[3], c->pf_hq, rows, f / 2, kBoxN);
+  if (!ok) return cudaErrorInvalidValue;
+  return cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGemm);
+}
+
+cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s) {
+  const int d = c->cfg.d_model, f = c->cfg.d_ff;
+  const int rows = (int)prefill_max_rows(c->cfg);
+  prefill_plan_kernel<<<1, 32, 0, s>>>(c->r);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  quant_x_kernel<<<(rows + 7) / 8, 256, 0, s>>>(c->r, x, d, c->pf_xq, c->pf_xsf, rows);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  GemmArgs g{};
+  g.r = c->r;
+  g.tsc = c->tsc;
+  g.status = c->status;
+  g.f = f;
+  g.d = d;
+  // gate/up + SwiGLU + h quantisation
+  g.sfa = c->pf_sfa_gu;
+  g.sfb = c->pf_xsf;
+  g.M = 2 * f;
+  g.K = d;
+  g.mode = 0;
+  g.hq_codes = c->pf_hq;
+  g.hq_sf = c->pf_hsf;
+  moe_gemm_kernel<<<c->sm_count, kGemmThreads, kSmemGemm, s>>>(c->pf_tm[0], c->pf_tm[2], g);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // down projection -> per-slot outputs
+  g.sfa = c->pf_sfa_dn;
+  g.sfb = c->pf_hsf;
+  g.M = d;
+  g.K = f;
+  g.mode = 1;
+  g.yexp = c->yexp;
+  moe_gemm_kernel<<<c->sm_count, kGemmThreads, kSmemGemm, s>>>(c->pf_tm[1], c->pf_tm[3], g);
+  (void)T;
+  return cudaGetLastError();
+}
+
+// h codes / scales of the last prefill, in slot order (see moe_debug_prefill_h)
+namespace {
+__global__ void gather_h_kernel(Routing r, int T, int k, int S, int f, const uint8_t* __restrict__ hq,
+                                const uint8_t* __restrict__ hsf, uint8_t* __restrict__ out_codes,
+                                uint8_t* __restrict__ out_sf) {
+  const int slot = blockIdx.x;
+  int pos;
+  if (slot < T * k) pos = r.slot_pos[slot];
+  else pos = slot;  // shared experts: positions T*k + s*T + t == slot
+  const int na = *r.n_active;
+  const int a = find_seg(r.act_pos, na, pos);
+  const int p = r.act_ppos[a] + (pos - r.act_pos[a]);
+  for (int i = threadIdx.x; i < f / 2; i += blockDim.x) out_codes[(size_t)slot * (f / 2) + i] = hq[(size_t)p * (f / 2) + i];
+  for (int b = threadIdx.x; b < f / 16; b += blockDim.x)
+    out_sf[(size_t)slot * (f / 16) + b] = hsf[sf_atom_offset(p, b, f / 64)];
+}
+}  // namespace
+
+cudaError_t launch_gather_prefill_h(const moe_ctx* c, int T, uint8_t* codes, uint8_t* sf, cudaStream_t s) {
+  const int slots = T * (c->cfg.top_k + c->cfg.n_shared);
+  if (slots == 0) return cudaSuccess;
+  gather_h_kernel<<<slots, 128, 0, s>>>(c->r, T, c->cfg.top_k, c->cfg.n_shared, c->cfg.d_ff, c->pf_hq, c->pf_hsf,
+                                        codes, sf);
+  return cudaGetLastError();
+}
+
+}  // namespace nvmoe
