@@ -1,21 +1,32 @@
-"""Benchmark of the NVFP4 sparse-MoE FFN layer on one B300 (or N replicas).
+"""Benchmark of the NVFP4 sparse-MoE FFN layer on one B300 (or N independent replicas).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode_b1|decode_b64|stack|prefill]
-                    [--impl ours|reference] [--no-cpu-baseline]
+    python bench.py [--gpus N] [--steps K] [--warmup W]
+                    [--workload decode_b1|decode_b64|stack|prefill] [--impl ours|reference]
+                    [--no-cpu-baseline]
 
-Default workload (decode_b1): batch-1 decode through one Flint-shaped MoE layer
-(d_model 2048, 256 routed experts top-6 + 1 shared, d_ff 512, NVFP4 weights
-quantised from N(0, 0.02), fp32 router 2048x256), one fresh bf16 token per
-step.  Sixteen independently seeded copies of the layer (7.3 GB, far above the
-126 MB L2) are used round-robin, so every step's weights come from HBM.
+Workloads (Flint-shaped layer: d_model 2048, 256 routed experts top-6 + 1
+shared, d_ff 512, NVFP4 weights quantised from N(0, 0.02), fp32 router 2048x256):
 
-A step is one whole pass of the layer (router, top-6, bucketing, experts,
-combine) over one token; steps are serialised, as in real decode.  K steps are
-captured in one CUDA graph and timed with CUDA events on the launching stream,
-bracketed by a barrier and a device synchronise.  Rank 0 prints one JSON line.
+  decode_b1  (default) batch-1 decode, one fresh bf16 token per step through one
+             layer.  Sixteen independently seeded copies of the layer (7.3 GB,
+             far above the 126 MB L2) are used round-robin, so every step's
+             weights come from HBM.
+  decode_b64 64 tokens per step, router skewed by a Zipf(1.1) per-expert bias
+             (~200 distinct experts per step); 16 layer copies as above.
+  stack      47 distinct MoE layers (~21 GB of NVFP4 experts) with the residual
+             add between them, one fresh token per step: a step is one token
+             through all 47 layers.
+  prefill    4096 tokens through one layer per step with the block-scaled FP4
+             tensor-core GEMMs; 16 layer copies.
 
-``--impl reference`` times the CPU oracle (the only reference this method
-has) on a bounded sample of the same workload and prints the same line with
+A step is one whole pass of the path (router, top-6, bucketing, experts,
+combine) over one batch; steps are serialised as in real decode.  A chunk of
+steps is captured in one CUDA graph and replayed until K steps have run, timed
+with CUDA events on the launching stream, bracketed by a barrier and a device
+synchronise.  Rank 0 prints one JSON line.
+
+``--impl reference`` times the CPU oracle (the only reference this method has)
+on a bounded sample of the same workload and prints the same line with
 "impl": "reference".
 """
 from __future__ import annotations
@@ -31,21 +42,36 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-EXPERT_BYTES = 3 * 2048 * 512 // 2 + 3 * 2048 * 512 // 16      # 1,769,472 B per Flint expert
-ROUTER_BYTES = 2048 * 256 * 4
+D_MODEL, N_EXP, TOP_K, D_FF, N_SHARED = 2048, 256, 6, 512, 1
+EXPERT_BYTES = 3 * D_MODEL * D_FF // 2 + 3 * D_MODEL * D_FF // 16   # 1,769,472 B per expert
+ROUTER_BYTES = D_MODEL * N_EXP * 4
+N_LAYERS_STACK = 47
+FLOP_PER_TOKEN = (TOP_K + N_SHARED) * 3 * 2 * D_MODEL * D_FF        # expert FLOPs per token
+FP4_OVER_BF16 = 13.5 / 2.25                                          # nominal dense ratio
+
+WORKLOADS = {
+    "decode_b1": dict(T=1, layers=16, steps=50000, chunk=1000,
+                      metric="MoE decode tok/s (batch-1, one Flint-shaped NVFP4 MoE layer)"),
+    "decode_b64": dict(T=64, layers=16, steps=2000, chunk=100,
+                       metric="MoE decode tok/s (batch-64 Zipf-skewed, one Flint-shaped NVFP4 MoE layer)"),
+    "stack": dict(T=1, layers=N_LAYERS_STACK, steps=512, chunk=1,
+                  metric="MoE decode tok/s (batch-1, 47-layer Flint MoE stack, attention omitted)"),
+    "prefill": dict(T=4096, layers=16, steps=40, chunk=4,
+                    metric="MoE prefill tok/s (4096 tokens, one Flint-shaped NVFP4 MoE layer)"),
+}
 
 
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
             p = json.load(fh)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
-        return 6400.0, "fallback"
+        return 6400.0, 1800.0, "fallback"
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms while running."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -56,10 +82,11 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            time.sleep(0.3)   # let the sampler start before the timed region
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -104,11 +131,12 @@ def _dist():
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def _build_layers(lib, torch, synth, n_copies, max_tokens, bias=None, seed0=0):
+def build_layers(lib, torch, synth, n_layers, max_tokens, bias=None, seed0=0):
+    """n independently seeded Flint-shaped layers, quantised on the device by the library."""
     s = synth.FLINT
     E = s.n_experts
     ctxs = []
-    for i in range(n_copies):
+    for i in range(n_layers):
         wg, wu, wd = synth.expert_weights(s, synth.layer_seed(seed0 + i), device="cuda")
         router = synth.router_weight(s, synth.router_seed(seed0 + i), device="cuda")
         weights = {"router": router, "router_bias": None if bias is None else bias.cuda()}
@@ -137,54 +165,77 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
+    wl = WORKLOADS[args.workload]
     s = synth.FLINT
-    K, W = args.steps, args.warmup
-    T = 64 if args.workload == "decode_b64" else 1
-    n_copies = int(os.environ.get("MOE_BENCH_COPIES", "16"))
-    bias = synth.zipf_bias(s, seed=4242) if T == 64 else None
-    ctxs = _build_layers(lib, torch, synth, n_copies, max_tokens=T, bias=bias, seed0=100 * rank)
+    T, n_layers = wl["T"], wl["layers"]
+    K, W = args.steps or wl["steps"], args.warmup
+    chunk = min(wl["chunk"], K)
+    replays = (K + chunk - 1) // chunk
+    K = replays * chunk
+    stack = args.workload == "stack"
+    prefill = args.workload == "prefill"
+    bias = synth.zipf_bias(s, seed=4242) if args.workload == "decode_b64" else None
+    ctxs = build_layers(lib, torch, synth, n_layers, max_tokens=T, bias=bias, seed0=100 * rank)
     stream = torch.cuda.Stream()
-    n_tok = (K + W) * T
-    xb, _ = synth.tokens(s, n_tok, seed=synth.token_seed(rank), device="cuda")
-    x = xb.view(K + W, T, s.d_model)
+    forward = lib.moe_forward_prefill if prefill else lib.moe_forward_decode
+    n_inputs = chunk + W                      # distinct token sets (chunk for the graph + warm-up)
+    xb, _ = synth.tokens(s, n_inputs * T, seed=synth.token_seed(rank), device="cuda")
+    x = xb.view(n_inputs, T, s.d_model)
     y = torch.empty_like(x)
+    bufs = [torch.empty((T, s.d_model), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
 
     def step(i, profile=None):
-        if profile is not None:
-            lib.moe_set_profile_events(ctxs[i % n_copies], *profile)
-        lib.moe_forward_decode(ctxs[i % n_copies], x[i], T, y[i], 0, stream)
-        if profile is not None:
-            lib.moe_set_profile_events(ctxs[i % n_copies], None, None)
+        """One step: one layer (single-layer workloads) or all layers with the residual (stack)."""
+        if not stack:
+            c = ctxs[i % n_layers]
+            if profile is not None:
+                lib.moe_set_profile_events(c, *profile)
+            forward(c, x[i], T, y[i], 0, stream)
+            if profile is not None:
+                lib.moe_set_profile_events(c, None, None)
+            return
+        cur = x[i]
+        for l, c in enumerate(ctxs):
+            out = y[i] if l == n_layers - 1 else bufs[l % 2]
+            if profile is not None and l == 0:
+                lib.moe_set_profile_events(c, profile[0], None)
+            if profile is not None and l == n_layers - 1:
+                lib.moe_set_profile_events(c, None, profile[1])
+            forward(c, cur, T, out, 1, stream)
+            if profile is not None and l in (0, n_layers - 1):
+                lib.moe_set_profile_events(c, None, None)
+            cur = out
 
     with torch.cuda.stream(stream):
-        for i in range(K, K + W):                # warm-up on inputs the timed steps never use
+        for i in range(chunk, chunk + W):          # warm-up on inputs the timed steps never use
             step(i)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for i in range(K):
+        for i in range(chunk):
             step(i)
     # per-kernel timing graph: events around the expert kernels of every step
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(chunk)]
     for a, b in ev:                               # events are created lazily at their first record
         a.record(stream)
         b.record(stream)
     torch.cuda.synchronize()
     gp = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gp, stream=stream):
-        for i in range(K):
+        for i in range(chunk):
             step(i, profile=ev[i])
-    for st in ctxs:
-        assert lib.moe_get_device_status(st) == 0
+    for c in ctxs:
+        assert lib.moe_get_device_status(c) == 0
 
-    def timed(graph):
+    def timed(graph, n):
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):          # replay() launches on the current stream
             a.record(stream)
-            graph.replay()
+            for _ in range(n):
+                graph.replay()
             b.record(stream)
         torch.cuda.synchronize()
         if world > 1:
@@ -192,76 +243,109 @@ def run_ours(args):
         return a.elapsed_time(b)
 
     with torch.cuda.stream(stream):
-        for _ in range(2):
-            g.replay()                            # graph warm-up
+        g.replay()                                # graph warm-up
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        ms = timed(g)
-        with torch.cuda.stream(stream):
-            gp.replay()
-        torch.cuda.synchronize()
-        kern_ms = sorted(a.elapsed_time(b) for a, b in ev)
+        ms = timed(g, replays)
+    with torch.cuda.stream(stream):
+        gp.replay()
+    torch.cuda.synchronize()
+    kern_ms = sorted(a.elapsed_time(b) for a, b in ev)
     if world > 1:
         t = torch.tensor([ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
 
-    # end to end: host (pinned) token in, host result out, every step
-    xh = x.cpu().pin_memory()
+    # end to end: pinned host tokens in, host result out, every step
+    xh = x[:chunk].cpu().pin_memory()
     yh = torch.empty_like(xh).pin_memory()
     xd = torch.empty((T, s.d_model), dtype=torch.bfloat16, device="cuda")
     yd = torch.empty_like(xd)
     ge = torch.cuda.CUDAGraph()
     with torch.cuda.graph(ge, stream=stream):
-        for i in range(K):
+        for i in range(chunk):
             xd.copy_(xh[i], non_blocking=True)
-            lib.moe_forward_decode(ctxs[i % n_copies], xd, T, yd, 0, stream)
+            if stack:
+                cur = xd
+                for l, c in enumerate(ctxs):
+                    out = yd if l == n_layers - 1 else bufs[l % 2]
+                    forward(c, cur, T, out, 1, stream)
+                    cur = out
+            else:
+                forward(ctxs[i % n_layers], xd, T, yd, 0, stream)
             yh[i].copy_(yd, non_blocking=True)
     with torch.cuda.stream(stream):
         ge.replay()
     torch.cuda.synchronize()
-    e2e_ms = timed(ge)
+    e2e_ms = timed(ge, replays)
     if world > 1:
         t = torch.tensor([e2e_ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t.item())
 
-    launches = K * lib.moe_kernels_per_forward(ctxs[0], T, 0)
+    per_fwd = lib.moe_kernels_per_forward(ctxs[0], T, int(prefill))
+    launches = K * per_fwd * (n_layers if stack else 1)
     for c in ctxs:
         lib.moe_destroy(c)
     if rank != 0:
         return
     tok = world * K * T
     value = tok / (ms / 1e3)
-    kmed = kern_ms[len(kern_ms) // 2]
     kavg = sum(kern_ms) / len(kern_ms)
-    peak, peak_kind = _peaks()
-    if T == 1:
-        alg_bytes = 7 * EXPERT_BYTES
-    else:
-        alg_bytes = None
-    achieved = alg_bytes / (kavg / 1e3) / 1e9 if alg_bytes else None
+    kmed = kern_ms[len(kern_ms) // 2]
+    hbm_peak, bf16_peak, peak_kind = _peaks()
     line = {
-        "metric": "MoE decode tok/s (batch-%d, one Flint-shaped NVFP4 MoE layer)" % T,
-        "value": round(value, 1), "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32 (nvfp4 weights, bf16 activations)", "data": "synthetic",
-        "config": {"workload": args.workload, "d_model": 2048, "n_experts": 256, "top_k": 6, "n_shared": 1,
-                   "d_ff": 512, "tokens_per_step": T, "layer_copies": n_copies,
-                   "l2": "16 rotating layer copies (7.3 GB > 126 MB L2); no weight re-read from L2",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "expert_kernels_us": {"avg": round(kavg * 1e3, 3), "median": round(kmed * 1e3, 3)},
-        "roofline": {"kernel": "expert kernels (gate/up+SwiGLU, down)", "bound": "hbm",
-                     "achieved": round(achieved, 1) if achieved else None, "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
-                     "peak_kind": peak_kind, "algorithmic_bytes_per_launch": alg_bytes, "traffic": None},
-        "e2e": {"value": round(tok / (e2e_ms / 1e3), 1), "unit": "tok/s",
-                "h2d_bytes_per_step": T * s.d_model * 2, "d2h_bytes_per_step": T * s.d_model * 2},
+        "metric": wl["metric"], "value": round(value, 1), "unit": "tok/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms / K, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 accumulate (nvfp4 weights, bf16 activations)"
+        if not prefill else "nvfp4 x nvfp4 -> f32 (tcgen05 block-scaled)", "data": "synthetic",
+        "config": {"workload": args.workload, "d_model": D_MODEL, "n_experts": N_EXP, "top_k": TOP_K,
+                   "n_shared": N_SHARED, "d_ff": D_FF, "tokens_per_step": T, "layers": n_layers,
+                   "l2": ("47 distinct layers, ~21 GB of weights" if stack else
+                          f"{n_layers} rotating layer copies (>= 7 GB, far above the 126 MB L2): "
+                          "no weight is re-read from L2 between steps"),
+                   "parallelism": "independent replicas" if world > 1 else "single GPU"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
+    if args.workload == "decode_b1":
+        alg = 7 * EXPERT_BYTES
+        ach = alg / (kavg / 1e3) / 1e9
+        line["roofline"] = {"kernel": "experts (gate/up + SwiGLU) and down/combine kernels, per token",
+                            "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                            "frac": round(ach / hbm_peak, 4), "peak_kind": peak_kind + " (copy, burst)",
+                            "algorithmic_bytes_per_launch": alg, "traffic": None,
+                            "expert_kernels_us": {"avg": round(kavg * 1e3, 3), "median": round(kmed * 1e3, 3)}}
+        line["expert_weight_gbs"] = round(alg * K / (ms / 1e3) / 1e9, 1)
+    elif args.workload == "stack":
+        alg = N_LAYERS_STACK * 7 * EXPERT_BYTES
+        ach = alg / (kavg / 1e3) / 1e9
+        line["roofline"] = {"kernel": "whole 47-layer token step (router, experts, down/combine per layer)",
+                            "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                            "frac": round(ach / hbm_peak, 4), "peak_kind": peak_kind + " (copy, burst)",
+                            "algorithmic_bytes_per_launch": alg, "traffic": None,
+                            "token_step_us": {"avg": round(kavg * 1e3, 3), "median": round(kmed * 1e3, 3)}}
+    elif prefill:
+        flop = FLOP_PER_TOKEN * T
+        tf = flop / (kavg / 1e3) / 1e12
+        fp4_peak = bf16_peak * FP4_OVER_BF16
+        wbytes = (N_EXP + N_SHARED) * EXPERT_BYTES
+        line["roofline"] = {"kernel": "prefill expert kernels (quantise x, gate/up GEMM, down GEMM)",
+                            "bound": "hbm", "achieved": round(wbytes / (kavg / 1e3) / 1e9, 1), "peak": hbm_peak,
+                            "unit": "GB/s", "frac": round(wbytes / (kavg / 1e3) / 1e9 / hbm_peak, 4),
+                            "peak_kind": peak_kind + " (copy, burst)",
+                            "algorithmic_bytes_per_launch": wbytes, "traffic": None,
+                            "tensor": {"achieved_tflops": round(tf, 1), "peak_tflops": round(fp4_peak, 1),
+                                       "frac": round(tf / fp4_peak, 4),
+                                       "peak_kind": "measured bf16 burst x nominal fp4/bf16 ratio 6"},
+                            "expert_kernels_us": {"avg": round(kavg * 1e3, 3), "median": round(kmed * 1e3, 3)}}
+        line["prefill_tflops"] = round(FLOP_PER_TOKEN * T * K / (ms / 1e3) / 1e12, 1)
+    else:
+        line["expert_kernels_us"] = {"avg": round(kavg * 1e3, 3), "median": round(kmed * 1e3, 3)}
+    line["e2e"] = {"value": round(tok / (e2e_ms / 1e3), 1), "unit": "tok/s",
+                   "h2d_bytes_per_step": T * D_MODEL * 2, "d2h_bytes_per_step": T * D_MODEL * 2}
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, T, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
 
 
@@ -277,19 +361,24 @@ def _blas_threads():
         return 1
 
 
-def cpu_baseline(workload: str, T: int, budget_s: float = 15.0):
-    """Time the oracle as it stands on a bounded sample of the decode workload:
-    tokens one at a time (T = 1) or one batch of T, weights of the chosen experts
-    quantised by the oracle beforehand (untimed, as moe_init is)."""
+def cpu_baseline(workload: str, budget_s: float = 15.0):
+    """Time the oracle as it stands on a bounded sample of the workload.
+
+    Weights of the experts the sample's tokens choose are quantised by the
+    oracle beforehand (untimed, as moe_init is); the timed part is the oracle's
+    forward pass.  decode_b1 / stack: 4 single-token steps through one layer
+    (the stack figure divides by 47 layers); decode_b64: one Zipf-skewed batch
+    of 8 tokens; prefill: 8 tokens through one layer in prefill mode."""
     import numpy as np
     import synth
     from oracle import moe as omoe
 
     s = synth.FLINT
+    T = {"decode_b1": 1, "stack": 1, "decode_b64": 8, "prefill": 8}[workload]
+    n_steps = 4 if T == 1 else 1
     router = synth.router_weight(s, synth.router_seed(0)).numpy()
-    bias = synth.zipf_bias(s, seed=4242).numpy() if T > 1 else None
-    n_steps = 8 if T == 1 else 1
-    xb, x = synth.tokens(s, n_steps * T, seed=synth.token_seed(0))
+    bias = synth.zipf_bias(s, seed=4242).numpy() if workload == "decode_b64" else None
+    _, x = synth.tokens(s, n_steps * T, seed=synth.token_seed(0))
     x = x.double().numpy().reshape(n_steps, T, s.d_model)
     cache = {}
 
@@ -319,27 +408,33 @@ def cpu_baseline(workload: str, T: int, budget_s: float = 15.0):
     t0 = time.perf_counter()
     done = 0
     for i in range(n_steps):
-        omoe.moe_layer(layers[i], x[i], s.top_k, s.n_shared)
+        omoe.moe_layer(layers[i], x[i], s.top_k, s.n_shared, prefill=(workload == "prefill"))
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(done * T / dt, 3), "unit": "tok/s", "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"{done} decode step(s) of {T} token(s) through one Flint-shaped layer "
-                      f"(numpy fp64 oracle, experts dequantised per step), {dt:.1f} s"}
+    per_layer = done * T / dt
+    value = per_layer / N_LAYERS_STACK if workload == "stack" else per_layer
+    what = {"decode_b1": "single-token decode steps through one layer",
+            "stack": "single-token decode steps through one layer, divided by 47 layers",
+            "decode_b64": "Zipf-skewed decode batch through one layer",
+            "prefill": "prefill-mode batch through one layer"}[workload]
+    return {"value": round(value, 4), "unit": "tok/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{done} x {T} token(s): {what} (numpy fp64 oracle, chosen experts dequantised "
+                      f"each step), {dt:.2f} s timed"}
 
 
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return
-    T = 64 if args.workload == "decode_b64" else 1
-    cb = cpu_baseline(args.workload, T, budget_s=args.cpu_budget)
-    line = {"impl": "reference", "metric": "MoE decode tok/s (batch-%d, one Flint-shaped NVFP4 MoE layer)" % T,
-            "value": cb["value"], "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "d_model": 2048, "n_experts": 256, "top_k": 6, "n_shared": 1,
-                       "d_ff": 512, "tokens_per_step": T},
+    wl = WORKLOADS[args.workload]
+    cb = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+    line = {"impl": "reference", "metric": wl["metric"], "value": cb["value"], "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps or wl["steps"], "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "d_model": D_MODEL, "n_experts": N_EXP, "top_k": TOP_K,
+                       "n_shared": N_SHARED, "d_ff": D_FF, "tokens_per_step": wl["T"], "layers": wl["layers"]},
             "cpu_baseline": cb,
             "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -348,9 +443,9 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="decode_b1", choices=["decode_b1", "decode_b64"])
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (default: per workload)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode_b1", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
