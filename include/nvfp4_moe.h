@@ -109,6 +109,37 @@ MOE_API moe_status moe_init(const moe_config* cfg, const moe_weights* weights, i
 MOE_API moe_status moe_route(moe_ctx* ctx, const void* x_bf16, int T, int32_t* idx, float* w,
                      int32_t* counts, cudaStream_t stream);
 
+/* Router without a context and without any allocation.  The Flint pages have
+ * no counterpart: it exists for callers that must not allocate device memory
+ * (for example a scheduler embedded in a runtime that owns every byte of the
+ * device through its own pool, which wants to know where tokens go -- to plan
+ * expert placement or prefetch -- before or without creating a layer context).
+ * Computes the same idx / w as moe_route, with the same kernels and the same
+ * summation order, so the two agree bit for bit on the same inputs.
+ *
+ *   x_bf16      [T][d_model] bf16, device
+ *   router      [d_model][n_experts] fp32, device;  router_bias [n_experts] fp32
+ *               device, or NULL for none
+ *   idx, w      [T][top_k] int32 / fp32 outputs, device, both required
+ *   d_model a multiple of 256 in 256..8192, 1 <= n_experts <= 256,
+ *   1 <= top_k <= min(8, n_experts); T == 0 does nothing.  A pointer the GPU
+ *   cannot dereference (plain pageable host memory) is MOE_ERR_INVALID_ARG.
+ *
+ * Scratch: the split-K partial logits live in one fixed device array of
+ * 1,048,576 fp32 (4 MiB) per device, inside the library's module.  A call needs
+ * nkc * T * n_experts elements of it, where nkc (1..64) is the router's K split
+ * for T; at n_experts = 256 every T up to 4096 fits.  A call that does not fit
+ * returns MOE_ERR_UNSUPPORTED before anything is queued.  Nothing in the array
+ * has to start at zero: each call writes every element it later reads.
+ * The array's device address is looked up (cudaGetSymbolAddress) on the first
+ * call on each device, with that device current; make that first call outside
+ * any stream capture.  Calls are asynchronous on `stream`; two calls that can
+ * run on the GPU at the same time (different streams, different host threads)
+ * share the one array and race -- order them on one stream or with events. */
+MOE_API moe_status moe_route_noalloc(const void* x_bf16, int T, const float* router,
+                             const float* router_bias, int d_model, int n_experts, int top_k,
+                             int32_t* idx, float* w, cudaStream_t stream);
+
 /* Decode form of the layer: activations stay exact (bf16 -> fp32), the NVFP4
  * weights are dequantised on the fly.  y [T][d_model] bf16 (may not alias x).
  * If `residual` is non-zero, y = bf16(x + layer(x)) (the stack's residual). */

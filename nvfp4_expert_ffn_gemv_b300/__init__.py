@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE_CHECK"}
 
 #: every symbol the C header declares
-EXPORTS = ("moe_init", "moe_route", "moe_forward_decode", "moe_forward_prefill", "moe_quantize_nvfp4",
+EXPORTS = ("moe_init", "moe_route", "moe_route_noalloc", "moe_forward_decode", "moe_forward_prefill", "moe_quantize_nvfp4",
            "moe_debug_prefill_h", "moe_set_profile_events", "moe_get_device_status",
            "moe_kernels_per_forward", "moe_destroy", "moe_status_string")
 
@@ -63,6 +63,7 @@ def _load():
     sig = {
         "moe_init": (i, [p(moe_config), p(moe_weights), i, p(vp)]),
         "moe_route": (i, [vp, vp, i, vp, vp, vp, vp]),
+        "moe_route_noalloc": (i, [vp, i, vp, vp, i, i, i, vp, vp, vp]),
         "moe_forward_decode": (i, [vp, vp, i, vp, i, vp]),
         "moe_forward_prefill": (i, [vp, vp, i, vp, i, vp]),
         "moe_quantize_nvfp4": (i, [vp, i, i, i, vp, vp, vp, vp]),
@@ -136,6 +137,13 @@ def moe_init(cfg: dict, weights: dict, device: int = 0):
 def moe_route(ctx, x, T: int, idx=None, w=None, counts=None, stream=None) -> None:
     _check("moe_route", _lib.moe_route(ctx, _ptr(x), int(T), _ptr(idx), _ptr(w), _ptr(counts),
                                        _stream(stream)))
+
+
+def moe_route_noalloc(x, T: int, router, router_bias, d_model: int, n_experts: int, top_k: int, idx, w,
+                      stream=None) -> None:
+    _check("moe_route_noalloc", _lib.moe_route_noalloc(_ptr(x), int(T), _ptr(router), _ptr(router_bias),
+                                                       int(d_model), int(n_experts), int(top_k), _ptr(idx),
+                                                       _ptr(w), _stream(stream)))
 
 
 def moe_forward_decode(ctx, x, T: int, y, residual: int = 0, stream=None) -> None:

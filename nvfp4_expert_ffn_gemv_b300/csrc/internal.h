@@ -73,6 +73,10 @@ cudaError_t launch_combine(const moe_ctx* c, const __nv_bfloat16* x, int T, __nv
 cudaError_t launch_quantize_nvfp4(const float* w, int n, int rows, int K, uint8_t* codes,
                                   uint8_t* scales, float* ts, cudaStream_t s);
 int router_chunks(int d, int T);
+// Allocation-free router (split-K partials in a static device array, see router.cu).
+size_t router_static_capacity();
+cudaError_t launch_router_static(const __nv_bfloat16* x, int T, const float* wr, const float* bias, int d,
+                                 int E, int K, int32_t* idx, float* w, cudaStream_t s);
 cudaError_t prepare_decode_kernels(const moe_ctx* c);
 bool prefill_supported(const moe_config& c);
 size_t prefill_max_rows(const moe_config& c);

@@ -304,6 +304,32 @@ moe_status moe_route(moe_ctx* x, const void* x_bf16, int T, int32_t* idx, float*
   return MOE_OK;
 }
 
+// True when the GPU can dereference p: device, managed or registered / pinned host memory.
+static bool device_reachable(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type != cudaMemoryTypeUnregistered;
+}
+
+moe_status moe_route_noalloc(const void* x_bf16, int T, const float* router, const float* router_bias,
+                             int d_model, int n_experts, int top_k, int32_t* idx, float* w, cudaStream_t s) {
+  if (T < 0 || d_model < 256 || d_model > 8192 || d_model % 256 != 0 || n_experts < 1 || n_experts > 256 ||
+      top_k < 1 || top_k > 8 || top_k > n_experts)
+    return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x_bf16 || !router || !idx || !w) return MOE_ERR_INVALID_ARG;
+  if (!device_reachable(x_bf16) || !device_reachable(router) || !device_reachable(idx) ||
+      !device_reachable(w) || (router_bias && !device_reachable(router_bias)))
+    return MOE_ERR_INVALID_ARG;
+  if ((size_t)router_chunks(d_model, T) * T * n_experts > router_static_capacity()) return MOE_ERR_UNSUPPORTED;
+  CK(launch_router_static(static_cast<const __nv_bfloat16*>(x_bf16), T, router, router_bias, d_model,
+                          n_experts, top_k, idx, w, s));
+  return MOE_OK;
+}
+
 moe_status moe_forward_decode(moe_ctx* x, const void* x_bf16, int T, void* y_bf16, int residual,
                               cudaStream_t s) {
   moe_status st = check_fwd(x, x_bf16, T, y_bf16);

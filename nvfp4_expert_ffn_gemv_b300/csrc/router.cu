@@ -13,6 +13,8 @@
 //   router_topk: one warp per token sums the partials in a fixed order
 //     (deterministic), adds the bias, runs k rounds of warp argmax over the
 //     (up to) 256 logits (8 per lane) and writes idx and the softmax weights.
+#include <atomic>
+
 #include "internal.h"
 
 namespace nvmoe {
@@ -133,6 +135,16 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
   }
 }
 
+// Scratch of the allocation-free router entry point: the split-K partial
+// logits [nkc][T][E] of one call.  Every element the top-k kernel reads is
+// written by the partial kernel of the same call, so nothing here has to start
+// at zero.  One copy per device: calls that overlap on the GPU race on it.
+constexpr size_t kStaticPartials = size_t(1) << 20;  // fp32 elements, 4 MiB
+static __device__ __align__(256) float g_static_partials[kStaticPartials];
+
+constexpr int kMaxCachedDevices = 64;
+std::atomic<float*> g_static_partials_addr[kMaxCachedDevices];
+
 }  // namespace
 
 int router_chunks(int d, int T) {
@@ -155,6 +167,28 @@ cudaError_t launch_router(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaS
   if (err != cudaSuccess) return err;
   router_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(c->router_partial, c->bias, c->has_bias, T, E,
                                                  c->cfg.top_k, nkc, c->r.idx, c->r.w, c->status);
+  return cudaGetLastError();
+}
+
+size_t router_static_capacity() { return kStaticPartials; }
+
+cudaError_t launch_router_static(const __nv_bfloat16* x, int T, const float* wr, const float* bias, int d,
+                                 int E, int K, int32_t* idx, float* w, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  float* part = dev < kMaxCachedDevices ? g_static_partials_addr[dev].load(std::memory_order_acquire)
+                                        : nullptr;
+  if (!part) {
+    err = cudaGetSymbolAddress((void**)&part, g_static_partials);
+    if (err != cudaSuccess) return err;
+    if (dev < kMaxCachedDevices) g_static_partials_addr[dev].store(part, std::memory_order_release);
+  }
+  const int nkc = router_chunks(d, T);
+  router_partial_kernel<<<dim3(nkc, (T + kTT - 1) / kTT), 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  router_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, bias, bias != nullptr, T, E, K, nkc, idx, w,
+                                                 nullptr);
   return cudaGetLastError();
 }
 
