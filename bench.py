@@ -167,7 +167,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     wl = WORKLOADS[args.workload]
     s = synth.FLINT
-    T, n_layers = wl["T"], wl["layers"]
+    T, n_layers = wl["T"], args.layers or wl["layers"]
     K, W = args.steps or wl["steps"], args.warmup
     chunk = min(wl["chunk"], K)
     replays = (K + chunk - 1) // chunk
@@ -299,7 +299,8 @@ def run_ours(args):
         "warmup": W, "ms_per_step": round(ms / K, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32 accumulate (nvfp4 weights, bf16 activations)"
         if not prefill else "nvfp4 x nvfp4 -> f32 (tcgen05 block-scaled)", "data": "synthetic",
-        "config": {"workload": args.workload, "d_model": D_MODEL, "n_experts": N_EXP, "top_k": TOP_K,
+        "config": {"workload": args.workload if n_layers == wl["layers"] else f"{args.workload} ({n_layers} layers)",
+                   "d_model": D_MODEL, "n_experts": N_EXP, "top_k": TOP_K,
                    "n_shared": N_SHARED, "d_ff": D_FF, "tokens_per_step": T, "layers": n_layers,
                    "l2": ("47 distinct layers, ~21 GB of weights" if stack else
                           f"{n_layers} rotating layer copies (>= 7 GB, far above the 126 MB L2): "
@@ -318,7 +319,7 @@ def run_ours(args):
                             "expert_kernels_us": {"avg": round(kavg * 1e3, 3), "median": round(kmed * 1e3, 3)}}
         line["expert_weight_gbs"] = round(alg * K / (ms / 1e3) / 1e9, 1)
     elif args.workload == "stack":
-        alg = N_LAYERS_STACK * 7 * EXPERT_BYTES
+        alg = n_layers * 7 * EXPERT_BYTES
         ach = alg / (kavg / 1e3) / 1e9
         line["roofline"] = {"kernel": "whole 47-layer token step (router, experts, down/combine per layer)",
                             "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
@@ -447,6 +448,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode_b1", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layer copies (default: per workload; smaller only for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()

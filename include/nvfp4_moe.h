@@ -131,9 +131,10 @@ MOE_API moe_status moe_route(moe_ctx* ctx, const void* x_bf16, int T, int32_t* i
  * for T; at n_experts = 256 every T up to 4096 fits.  A call that does not fit
  * returns MOE_ERR_UNSUPPORTED before anything is queued.  Nothing in the array
  * has to start at zero: each call writes every element it later reads.
- * The array's device address is looked up (cudaGetSymbolAddress) on the first
- * call on each device, with that device current; make that first call outside
- * any stream capture.  Calls are asynchronous on `stream`; two calls that can
+ * On the first call on each device (with that device current) the array's
+ * device address is looked up (cudaGetSymbolAddress) and the router kernel's
+ * shared-memory limit is raised (cudaFuncSetAttribute); make that first call
+ * outside any stream capture.  Calls are asynchronous on `stream`; two calls that can
  * run on the GPU at the same time (different streams, different host threads)
  * share the one array and race -- order them on one stream or with events. */
 MOE_API moe_status moe_route_noalloc(const void* x_bf16, int T, const float* router,

@@ -38,6 +38,11 @@ struct moe_ctx {
   int* status = nullptr;     // device status word
   int max_positions = 0;
 
+  // batched decode on the tensor cores (see decode_mma.cu)
+  int mma_enabled = 0;
+  uint8_t* x16 = nullptr;        // [max_tokens][d] f16, prescaled, k-permuted
+  float* xunshift = nullptr;     // [max_tokens]
+
   // batch-1 decode fast path (see decode_b1.cu / repack.cu)
   int b1_enabled = 0;
   int b1_grid = 0, b1_rmax = 0, b1_nbmax = 0;
@@ -73,11 +78,15 @@ cudaError_t launch_combine(const moe_ctx* c, const __nv_bfloat16* x, int T, __nv
 cudaError_t launch_quantize_nvfp4(const float* w, int n, int rows, int K, uint8_t* codes,
                                   uint8_t* scales, float* ts, cudaStream_t s);
 int router_chunks(int d, int T);
+cudaError_t prepare_router_kernels();
 // Allocation-free router (split-K partials in a static device array, see router.cu).
 size_t router_static_capacity();
 cudaError_t launch_router_static(const __nv_bfloat16* x, int T, const float* wr, const float* bias, int d,
                                  int E, int K, int32_t* idx, float* w, cudaStream_t s);
 cudaError_t prepare_decode_kernels(const moe_ctx* c);
+bool mma_decode_supported(const moe_config& c);
+cudaError_t prepare_mma_decode(const moe_ctx* c);
+cudaError_t launch_mma_decode(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
 bool prefill_supported(const moe_config& c);
 size_t prefill_max_rows(const moe_config& c);
 cudaError_t prefill_prepare(moe_ctx* c);

@@ -86,6 +86,10 @@ size_t carve(moe_ctx* x, uint8_t* base) {
     x->ticket = cv.take<unsigned>(base, 4);
   }
   x->max_positions = (int)P;
+  if (x->mma_enabled) {
+    x->x16 = cv.take<uint8_t>(base, T * d * 2);
+    x->xunshift = cv.take<float>(base, T);
+  }
   if (x->pf_enabled) {
     const size_t rows = prefill_max_rows(c);
     x->pf_sfa_gu = cv.take<uint8_t>(base, n * 2 * f * d / 16);
@@ -185,6 +189,7 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
                             &x->b1_smem);
   }
   x->pf_enabled = prefill_supported(c);
+  x->mma_enabled = mma_decode_supported(c);
   x->arena_bytes = carve(x, nullptr);
   if (cudaMalloc(&x->arena, x->arena_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -253,7 +258,9 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
                     : cudaMemset(x->bias, 0, E * sizeof(float));
   }
   if (e == cudaSuccess) e = cudaMemset(x->status, 0, sizeof(int));
+  if (e == cudaSuccess) e = prepare_router_kernels();
   if (e == cudaSuccess) e = prepare_decode_kernels(x);
+  if (e == cudaSuccess && x->mma_enabled) e = prepare_mma_decode(x);
   if (e == cudaSuccess && x->pf_enabled) {
     e = prefill_prepare(x);
     if (e == cudaSuccess) e = cudaMemset(x->pf_hq, 0, prefill_max_rows(c) * (f / 2));
@@ -349,8 +356,12 @@ moe_status moe_forward_decode(moe_ctx* x, const void* x_bf16, int T, void* y_bf1
   CK(launch_router(x, xb, T, s));
   CK(launch_bucket(x, T, s));
   if (x->prof_start) CK(cudaEventRecordWithFlags(x->prof_start, s, cudaEventRecordExternal));
-  CK(launch_gateup_decode(x, xb, T, s));
-  CK(launch_down_decode(x, T, s));
+  if (x->mma_enabled) {
+    CK(launch_mma_decode(x, xb, T, s));
+  } else {
+    CK(launch_gateup_decode(x, xb, T, s));
+    CK(launch_down_decode(x, T, s));
+  }
   if (x->prof_stop) CK(cudaEventRecordWithFlags(x->prof_stop, s, cudaEventRecordExternal));
   CK(launch_combine(x, xb, T, static_cast<__nv_bfloat16*>(y_bf16), residual, s));
   return MOE_OK;
@@ -416,6 +427,7 @@ int moe_kernels_per_forward(moe_ctx* x, int T, int prefill) {
   if (!x || T <= 0) return 0;
   if (!prefill && T == 1 && x->b1_enabled) return 3;
   if (prefill) return 8;   // router x2, bucket, plan, quantise x, GEMM x2, combine
+  if (x->mma_enabled) return 7;   // router x2, bucket, x prescale, gate/up, down, combine
   return 6;
 }
 

@@ -9,22 +9,24 @@
 // expert), so it runs on the tensor cores with both operands in NVFP4:
 //
 //   1. plan:   padded position blocks per active expert (multiples of 128
-//              tokens) and the prefix of 256-token N tiles;
+//              tokens, so every 128-row block belongs to one expert);
 //   2. x -> NVFP4 (16-element E4M3 block scales, tensor scale 1) gathered into
 //              the padded blocks, scales written straight into the
 //              scale-factor atoms the MMA reads;
-//   3. GEMM gate/up, swap-AB: D[128 weight rows, N tokens] per (expert,
-//              128-row tile, N tile); the 128-row tile of the gate/up layout
-//              holds 64 gate rows and the matching 64 up rows, so the epilogue
-//              forms h = silu(g) * u for 64 hidden units and quantises it
-//              to NVFP4 (again block 16, scale 1) into the second GEMM's
-//              operand layout;
-//   4. GEMM down: D[128 output dims, N tokens] * ts_down -> per-slot rows of
+//   3. GEMM gate/up: D[128 tokens, 128 weight rows] per (token block, 128-row
+//              tile of the gate/up layout).  Such a tile holds 64 gate rows
+//              and the matching 64 up rows, so each epilogue thread (one
+//              token, one TMEM lane) forms h = silu(g) * u for 64 hidden units
+//              in registers and quantises it to NVFP4 (block 16, scale 1):
+//              32 contiguous code bytes and 4 adjacent scale bytes per token;
+//   4. GEMM down: D[128 tokens, 128 output dims] * ts_down -> per-slot rows of
 //              yexp (fp32), then the decode path's fixed-order combine.
 //
-// GEMM kernel: persistent, one CTA (192 threads) per SM, 512 TMEM columns.
-//   warp 0  TMA producer: 3-stage ring of {A 128x256 fp4 (SW128), B <=256x256
-//           fp4 (SW128, 32-row boxes), SFA 4 atoms, SFB 4-8 atoms}
+// GEMM kernel: persistent, one CTA (192 threads) per SM, 512 TMEM columns
+// (two 128-column accumulators, so the epilogue of one tile overlaps the MMAs
+// of the next, plus 4 stages x 32 scale-factor columns).
+//   warp 0  TMA producer: 4-stage ring of {A 128x256 fp4 tokens (SW128),
+//           B 128x256 fp4 weights (SW128), SFA 4 atoms, SFB 4 atoms}
 //   warp 1  TMEM owner + single-thread MMA issuer: per stage, scale atoms ->
 //           TMEM (tcgen05.cp 32x128b.warpx4), 4 MMAs of K = 64
 //   warps 2-5 epilogue (TMEM lanes 32*(warp%4) ..), tcgen05.ld 32 columns
@@ -42,27 +44,25 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kBM = 128;        // weight rows per tile
+constexpr int kBM = 128;        // tokens per tile (MMA M, TMEM lanes)
+constexpr int kBN = 128;        // weight rows per tile (MMA N)
 constexpr int kStageK = 256;    // fp4 elements of K per stage (128 bytes per row)
-constexpr int kStages = 3;
-constexpr int kMaxN = 256;      // tokens per N tile
-constexpr int kBoxN = 32;       // rows per TMA box of the activation operand
+constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSfCol0 = 256;    // scale-factor columns start after D
-constexpr int kSfColsPerStage = 48;  // SFA 4 k-steps x 4 + SFB 4 k-steps x 8
+constexpr int kSfCol0 = 2 * kBN;      // scale-factor columns after the two accumulators
+constexpr int kSfColsPerStage = 32;   // SFA 4 k-steps x 4 + SFB 4 k-steps x 4
 
 // shared-memory plan of the GEMM kernel (offsets from a 1024-aligned base)
 constexpr int kA = kBM * 128;                 // 16 KB per stage
-constexpr int kB = kMaxN * 128;               // 32 KB per stage
-constexpr int kSFA = 4 * 512;                 // 2 KB
-constexpr int kSFB = 2 * 4 * 512;             // 4 KB
+constexpr int kB = kBN * 128;                 // 16 KB per stage
+constexpr int kSF = 4 * 512;                  // 2 KB per operand per stage
+constexpr int kStageBytes = kA + kB + 2 * kSF;
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kA;
 constexpr int kOffSFA = kOffB + kStages * kB;
-constexpr int kOffSFB = kOffSFA + kStages * kSFA;
-constexpr int kOffU = kOffSFB + kStages * kSFB;     // 64 x 32 fp32 exchange buffer
-constexpr int kSmemGemm = kOffU + 64 * 32 * 4 + 1024;  // + alignment slack
+constexpr int kOffSFB = kOffSFA + kStages * kSF;
+constexpr int kSmemGemm = kOffSFB + kStages * kSF + 1024;  // + alignment slack
 
 // ---------------------------------------------------------------------------
 // plan: padded positions and N-tile prefix per active expert (one warp)
@@ -70,28 +70,21 @@ constexpr int kSmemGemm = kOffU + 64 * 32 * 4 + 1024;  // + alignment slack
 __global__ void prefill_plan_kernel(Routing r) {
   const int lane = threadIdx.x;
   const int na = *r.n_active;
-  int pp = 0, nt = 0;
+  int pp = 0;
   for (int base = 0; base < na; base += 32) {
     const int a = base + lane;
     const int n = a < na ? r.act_n[a] : 0;
-    int vp = (n + 127) / 128 * 128, vt = (n + kMaxN - 1) / kMaxN;
-    int ip = vp, it = vt;
+    const int vp = (n + 127) / 128 * 128;
+    int ip = vp;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int up = __shfl_up_sync(0xffffffffu, ip, o), ut = __shfl_up_sync(0xffffffffu, it, o);
-      if (lane >= o) { ip += up; it += ut; }
+      const int up = __shfl_up_sync(0xffffffffu, ip, o);
+      if (lane >= o) ip += up;
     }
-    if (a < na) {
-      r.act_ppos[a] = pp + ip - vp;
-      r.act_ntb[a] = nt + it - vt;
-    }
+    if (a < na) r.act_ppos[a] = pp + ip - vp;
     pp += __shfl_sync(0xffffffffu, ip, 31);
-    nt += __shfl_sync(0xffffffffu, it, 31);
   }
-  if (lane == 0) {
-    r.act_ppos[na] = pp;
-    r.act_ntb[na] = nt;
-  }
+  if (lane == 0) r.act_ppos[na] = pp;
 }
 
 // largest a < na with tab[a] <= v (tab non-decreasing, tab[0] = 0)
@@ -180,8 +173,8 @@ __global__ void __launch_bounds__(256) quant_x_kernel(Routing r, const __nv_bflo
 // ---------------------------------------------------------------------------
 struct GemmArgs {
   Routing r;
-  const uint8_t* sfa;     // weight scale atoms [n_all][mtiles][ksteps][512]
-  const uint8_t* sfb;     // activation scale atoms [rows/128][ksteps][512]
+  const uint8_t* sfa;     // activation scale atoms [rows/128][K/64][512]
+  const uint8_t* sfb;     // weight scale atoms [n_all][M/128][K/64][512]
   const float* tsc;       // [n_all][3]
   int M;                  // weight rows per expert (2f or d)
   int K;                  // contraction length
@@ -196,48 +189,64 @@ struct GemmArgs {
   int* status;
 };
 
+// unit u -> (128-token block, 128-row weight tile)
 struct UnitInfo {
-  int a, e, n0, N, nmma, mt, pos0, nbox, natoms;
+  int a, e, p0, nt, ntile;
 };
 
-__device__ __forceinline__ UnitInfo decode_unit(const GemmArgs& g, int u, int mtiles, int na) {
+__device__ __forceinline__ UnitInfo decode_unit(const GemmArgs& g, int u, int ntiles, int na) {
   UnitInfo ui;
-  const int ntg = u / mtiles;
-  ui.mt = u % mtiles;
-  ui.a = find_seg(g.r.act_ntb, na, ntg);
-  const int nt = ntg - g.r.act_ntb[ui.a];
+  const int tb = u / ntiles;
+  ui.ntile = u % ntiles;
+  ui.p0 = tb * kBM;
+  ui.a = find_seg(g.r.act_ppos, na, ui.p0);
   ui.e = g.r.act_e[ui.a];
-  const int n = g.r.act_n[ui.a];
-  ui.n0 = g.r.act_ppos[ui.a] + nt * kMaxN;
-  ui.N = min(kMaxN, n - nt * kMaxN);
-  ui.nmma = (ui.N + 15) / 16 * 16;
-  ui.pos0 = g.r.act_pos[ui.a] + nt * kMaxN;
-  ui.nbox = (ui.N + kBoxN - 1) / kBoxN;
-  ui.natoms = (ui.N + 127) / 128;
+  ui.nt = min(kBM, g.r.act_n[ui.a] - (ui.p0 - g.r.act_ppos[ui.a]));   // real tokens in the block
   return ui;
 }
 
 __device__ __forceinline__ float silu_acc(float z) { return z / (1.0f + expf(-z)); }
 
+// NVFP4 (scale 1) of 16 consecutive fp32 values held by one thread -> 8 code bytes, one scale byte
+__device__ __forceinline__ uint32_t quant16(const float* v, uint2& codes) {
+  float amax = 0.f;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+  const uint32_t s = q_e4m3(__fdiv_rn(amax, 6.0f));
+  const float dq = e4m3_to_f32(s);
+  uint32_t lo = 0, hi = 0;
+  if (dq > 0.f) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      lo |= q_e2m1x2(__fdiv_rn(v[2 * q], dq), __fdiv_rn(v[2 * q + 1], dq)) << (8 * q);
+      hi |= q_e2m1x2(__fdiv_rn(v[8 + 2 * q], dq), __fdiv_rn(v[8 + 2 * q + 1], dq)) << (8 * q);
+    }
+  }
+  codes = make_uint2(lo, hi);
+  return s;
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], dfull_bar, dempty_bar;
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], dfull_bar[2], dempty_bar[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int na = *g.r.n_active;
-  const int mtiles = g.M / kBM, ksteps = g.K / 64, kstages = g.K / kStageK;
-  const int U = g.r.act_ntb[na] * mtiles;
+  const int ntiles = g.M / kBN, ksteps = g.K / 64, kstages = g.K / kStageK;
+  const int U = (g.r.act_ppos[na] / kBM) * ntiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(&dfull_bar, 1);
-    mbar_init(&dempty_bar, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&dfull_bar[b], 1);
+      mbar_init(&dempty_bar[b], 4);
+    }
     abort_flag = 0;
     fence_barrier_init();
   }
@@ -265,21 +274,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
-        const UnitInfo ui = decode_unit(g, u, mtiles, na);
-        const int arow = ui.e * g.M + ui.mt * kBM;
+        const UnitInfo ui = decode_unit(g, u, ntiles, na);
+        const int brow = ui.e * g.M + ui.ntile * kBN;
+        const uint8_t* sfa = g.sfa + (size_t)(ui.p0 / kBM) * ksteps * 512;
+        const uint8_t* sfb = g.sfb + ((size_t)ui.e * ntiles + ui.ntile) * ksteps * 512;
         for (int ks = 0; ks < kstages; ++ks) {
           if (!bounded_wait(&empty_bar[stage], phase ^ 1)) break;
-          const uint32_t bytes = kA + ui.nbox * kBoxN * 128 + kSFA + ui.natoms * 4 * 512;
-          mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          tma_load_2d(smem + kOffA + stage * kA, &tmA, ks * 128, arow, &full_bar[stage]);
-          for (int b = 0; b < ui.nbox; ++b)
-            tma_load_2d(smem + kOffB + stage * kB + b * kBoxN * 128, &tmB, ks * 128, ui.n0 + b * kBoxN,
-                        &full_bar[stage]);
-          bulk_load(smem + kOffSFA + stage * kSFA,
-                    g.sfa + (((size_t)ui.e * mtiles + ui.mt) * ksteps + ks * 4) * 512, kSFA, &full_bar[stage]);
-          for (int at = 0; at < ui.natoms; ++at)
-            bulk_load(smem + kOffSFB + stage * kSFB + at * 2048,
-                      g.sfb + (((size_t)(ui.n0 >> 7) + at) * ksteps + ks * 4) * 512, 2048, &full_bar[stage]);
+          mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+          tma_load_2d(smem + kOffA + stage * kA, &tmA, ks * 128, ui.p0, &full_bar[stage]);
+          tma_load_2d(smem + kOffB + stage * kB, &tmB, ks * 128, brow, &full_bar[stage]);
+          bulk_load(smem + kOffSFA + stage * kSF, sfa + (size_t)ks * 4 * 512, kSF, &full_bar[stage]);
+          bulk_load(smem + kOffSFB + stage * kSF, sfb + (size_t)ks * 4 * 512, kSF, &full_bar[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -288,103 +293,101 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------ MMA issuer ----------------------------
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0, dphase = 0;
-      for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
-        const UnitInfo ui = decode_unit(g, u, mtiles, na);
-        if (!bounded_wait(&dempty_bar, dphase ^ 1)) break;
-        dphase ^= 1;
+      uint32_t phase = 0;
+      const uint32_t idesc = idesc_mxf4nvf4(kBM, kBN);
+      int i = 0;
+      for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x, ++i) {
+        const int buf = i & 1;
+        if (!bounded_wait(&dempty_bar[buf], ((i >> 1) & 1) ^ 1)) break;
         tc_fence_after();
-        const uint32_t idesc = idesc_mxf4nvf4(kBM, ui.nmma);
+        const uint32_t d_tmem = tmem + buf * kBN;
         for (int ks = 0; ks < kstages; ++ks) {
           if (!bounded_wait(&full_bar[stage], phase)) break;
           tc_fence_after();
           const uint32_t sf = tmem + kSfCol0 + stage * kSfColsPerStage;
-          const uint32_t sa = smem_u32(smem + kOffSFA + stage * kSFA);
-          const uint32_t sb = smem_u32(smem + kOffSFB + stage * kSFB);
+          const uint32_t sa = smem_u32(smem + kOffSFA + stage * kSF);
+          const uint32_t sb = smem_u32(smem + kOffSFB + stage * kSF);
+#pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             tmem_cp_sf_atom(sf + kk * 4, desc_sf_atom(sa + kk * 512));
-            for (int at = 0; at < ui.natoms; ++at)
-              tmem_cp_sf_atom(sf + 16 + kk * 8 + at * 4, desc_sf_atom(sb + at * 2048 + kk * 512));
+            tmem_cp_sf_atom(sf + 16 + kk * 4, desc_sf_atom(sb + kk * 512));
           }
           const uint64_t adesc = desc_kmajor_sw128(smem_u32(smem + kOffA + stage * kA));
           const uint64_t bdesc = desc_kmajor_sw128(smem_u32(smem + kOffB + stage * kB));
+#pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_mxf4nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, sf + kk * 4,
-                         sf + 16 + kk * 8, ks > 0 || kk > 0);
+            mma_mxf4nvf4(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, sf + kk * 4,
+                         sf + 16 + kk * 4, ks > 0 || kk > 0);
           tc_commit(&empty_bar[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
-        tc_commit(&dfull_bar);
+        tc_commit(&dfull_bar[buf]);
       }
     }
   } else {
     // ------------------------------ epilogue ------------------------------
-    const int q = warp & 3;              // TMEM lane quadrant
-    const int m = q * 32 + lane;         // tile row held by this thread
-    float* ubuf = reinterpret_cast<float*>(smem + kOffU);
-    uint32_t dphase = 0;
-    // Every epilogue warp runs the same units and column chunks and never leaves
-    // the loop early (a failed wait only skips the work), so the named-barrier
-    // counts of the four warps always match.
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-      const UnitInfo ui = decode_unit(g, u, mtiles, na);
-      const bool ok = bounded_wait(&dfull_bar, dphase);
-      dphase ^= 1;
+    // TMEM lane = token row of the block; this thread owns token row m.
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    int i = 0;
+    // Every epilogue warp runs the same units and never leaves the loop early
+    // (a failed wait only skips the work), so all four always arrive.
+    for (int u = blockIdx.x; u < U; u += gridDim.x, ++i) {
+      const UnitInfo ui = decode_unit(g, u, ntiles, na);
+      const int buf = i & 1;
+      const bool ok = bounded_wait(&dfull_bar[buf], (i >> 1) & 1);
       tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * kBN;
       const float* ts = g.tsc + ui.e * 3;
-      for (int c0 = 0; c0 < ui.nmma; c0 += 32) {
-        uint32_t v[32];
-        if (ok) {
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
-        } else {
+      const int p = ui.p0 + m;                    // padded row of this token
+      if (g.mode == 0) {
+        // columns 0..63 gate rows, 64..127 up rows of hidden units 64*ntile + 0..63
+        const float tg = ts[0], tu = ts[1];
+        uint32_t sc4 = 0;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t gv[32], uv[32];
+          if (ok) {
+            tmem_ld32(taddr + half * 32, gv);
+            tmem_ld32(taddr + 64 + half * 32, uv);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0u;
+            for (int j = 0; j < 32; ++j) { gv[j] = 0u; uv[j] = 0u; }
+          }
+          float hv[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            hv[j] = silu_acc(__uint_as_float(gv[j]) * tg) * (__uint_as_float(uv[j]) * tu);
+          uint2 c0, c1;
+          const uint32_t s0 = quant16(hv, c0), s1 = quant16(hv + 16, c1);
+          sc4 |= (s0 | (s1 << 8)) << (16 * half);
+          if (ok)
+            *reinterpret_cast<uint4*>(g.hq_codes + (size_t)p * (g.f / 2) + ui.ntile * 32 + half * 16) =
+                make_uint4(c0.x, c0.y, c1.x, c1.y);
         }
-        if (g.mode == 0) {
-          // rows 0..63 gate, 64..127 up (same hidden units); quadrants 2,3 hand their up values over
-          if (q >= 2) {
+        // the 4 block scales of these 64 hidden units are one k-step of the down GEMM: 4 adjacent bytes
+        if (ok) *reinterpret_cast<uint32_t*>(g.hq_sf + sf_atom_offset(p, ui.ntile * 4, g.f / 64)) = sc4;
+      } else {
+        const int i_tok = p - g.r.act_ppos[ui.a];   // index among the expert's tokens
+        const bool real = ok && m < ui.nt;
+        const float td = ts[2];
+        float* dst = g.yexp + (size_t)(g.r.act_pos[ui.a] + i_tok) * g.d + ui.ntile * kBN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+          uint32_t v[32];
+          if (ok) tmem_ld32(taddr + c0, v);
+          if (real) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) ubuf[(m - 64) * 32 + j] = __uint_as_float(v[j]);
-          }
-          asm volatile("bar.sync 1, 128;" ::: "memory");
-          if (q < 2) {
-            const int jh = ui.mt * 64 + m;      // hidden unit
-            const int b = jh >> 4;              // its 16-block along d_ff
-            const int fsteps = g.f / 64;
-#pragma unroll 4
-            for (int j = 0; j < 32; ++j) {
-              const float gg = __uint_as_float(v[j]) * ts[0];
-              const float uu = ubuf[m * 32 + j] * ts[1];
-              const float h = silu_acc(gg) * uu;
-              // block amax over the 16 lanes that hold this token's 16 hidden units
-              float am = fabsf(h);
-#pragma unroll
-              for (int o = 1; o < 16; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-              const uint32_t s = q_e4m3(__fdiv_rn(am, 6.0f));
-              const float dq = e4m3_to_f32(s);
-              const float hn = dq > 0.f ? __fdiv_rn(h, dq) : 0.f;
-              const float partner = __shfl_xor_sync(0xffffffffu, hn, 1);
-              const int p = ui.n0 + c0 + j;     // padded row of this token
-              if (ok && (lane & 1) == 0) {
-                const uint32_t byte = dq > 0.f ? q_e2m1x2(hn, partner) : 0u;
-                g.hq_codes[(size_t)p * (g.f / 2) + (jh >> 1)] = static_cast<uint8_t>(byte);
-              }
-              if (ok && (lane & 15) == 0) g.hq_sf[sf_atom_offset(p, b, fsteps)] = static_cast<uint8_t>(s);
-            }
-          }
-          asm volatile("bar.sync 1, 128;" ::: "memory");
-        } else {
-          const int rdim = ui.mt * kBM + m;
-#pragma unroll 8
-          for (int j = 0; j < 32; ++j) {
-            if (ok && c0 + j < ui.N)
-              g.yexp[(size_t)(ui.pos0 + c0 + j) * g.d + rdim] = __uint_as_float(v[j]) * ts[2];
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(dst + c0 + j) =
+                  make_float4(__uint_as_float(v[j]) * td, __uint_as_float(v[j + 1]) * td,
+                              __uint_as_float(v[j + 2]) * td, __uint_as_float(v[j + 3]) * td);
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0 && ok) mbar_arrive(&dempty_bar);
+      if (lane == 0 && ok) mbar_arrive(&dempty_bar[buf]);
     }
   }
 
@@ -464,8 +467,8 @@ cudaError_t prefill_prepare(moe_ctx* c) {
   const size_t rows = prefill_max_rows(c->cfg);
   bool ok = make_tmap(&c->pf_tm[0], c->gu_codes, (uint64_t)n * 2 * f, d / 2, kBM) &&
             make_tmap(&c->pf_tm[1], c->dn_codes, (uint64_t)n * d, f / 2, kBM) &&
-            make_tmap(&c->pf_tm[2], c->pf_xq, rows, d / 2, kBoxN) &&
-            make_tmap(&c->pf_tm[3], c->pf_hq, rows, f / 2, kBoxN);
+            make_tmap(&c->pf_tm[2], c->pf_xq, rows, d / 2, kBM) &&
+            make_tmap(&c->pf_tm[3], c->pf_hq, rows, f / 2, kBM);
   if (!ok) return cudaErrorInvalidValue;
   return cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGemm);
 }
@@ -485,23 +488,23 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   g.f = f;
   g.d = d;
   // gate/up + SwiGLU + h quantisation
-  g.sfa = c->pf_sfa_gu;
-  g.sfb = c->pf_xsf;
+  g.sfa = c->pf_xsf;
+  g.sfb = c->pf_sfa_gu;
   g.M = 2 * f;
   g.K = d;
   g.mode = 0;
   g.hq_codes = c->pf_hq;
   g.hq_sf = c->pf_hsf;
-  moe_gemm_kernel<<<c->sm_count, kGemmThreads, kSmemGemm, s>>>(c->pf_tm[0], c->pf_tm[2], g);
+  moe_gemm_kernel<<<c->sm_count, kGemmThreads, kSmemGemm, s>>>(c->pf_tm[2], c->pf_tm[0], g);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // down projection -> per-slot outputs
-  g.sfa = c->pf_sfa_dn;
-  g.sfb = c->pf_hsf;
+  g.sfa = c->pf_hsf;
+  g.sfb = c->pf_sfa_dn;
   g.M = d;
   g.K = f;
   g.mode = 1;
   g.yexp = c->yexp;
-  moe_gemm_kernel<<<c->sm_count, kGemmThreads, kSmemGemm, s>>>(c->pf_tm[1], c->pf_tm[3], g);
+  moe_gemm_kernel<<<c->sm_count, kGemmThreads, kSmemGemm, s>>>(c->pf_tm[3], c->pf_tm[1], g);
   (void)T;
   return cudaGetLastError();
 }

@@ -7,12 +7,14 @@
 // renormalised, ties broken towards the lower expert index.
 //
 // Two kernels:
-//   router_partial: split-K GEMV/GEMM.  Block (kc, tile) multiplies a tile of 8
-//     tokens by the K-chunk kc of W_r [d][E]; thread e owns expert e, so every
-//     W_r row is read as one coalesced 1 KB line.  Partial sums go to scratch.
-//   router_topk: one warp per token sums the partials in a fixed order
-//     (deterministic), adds the bias, runs k rounds of warp argmax over the
-//     (up to) 256 logits (8 per lane) and writes idx and the softmax weights.
+//   router_partial: split-K GEMV/GEMM.  Block (kc, tile) multiplies a tile of TT
+//     tokens (8, or 32 from 256 tokens up) by the K-chunk kc of W_r [d][E];
+//     thread e owns expert e, so every W_r row is read as one coalesced 1 KB
+//     line and feeds TT FMAs.  Partial sums go to scratch.
+//   router_topk: one CTA per token; thread e sums its nkc partials in a fixed
+//     order (deterministic) and adds the bias, then one warp runs k rounds of
+//     argmax over the (up to) 256 logits (8 per lane) and writes idx and the
+//     softmax weights.
 #include <atomic>
 
 #include "internal.h"
@@ -21,41 +23,150 @@ namespace nvmoe {
 
 namespace {
 
-constexpr int kTT = 8;      // tokens per router tile
 constexpr int kSlab = 256;  // rows of W_r staged per x slab
 
+// Transposed x slab xs[kk][t] (row stride TT + 4) for k0 <= k < k0 + slab:
+// thread kk (blockDim == kSlab) loads its TT values at once, so all of a
+// thread's L2 loads are in flight together.
+template <int TT>
+__device__ __forceinline__ void stage_x_slab(const __nv_bfloat16* __restrict__ x, int d, int t0, int nt, int k0,
+                                             int slab, float* xs) {
+  const int kk = threadIdx.x;
+  float v[TT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+    v[t] = (t < nt && kk < slab) ? __bfloat162float(x[(size_t)(t0 + t) * d + k0 + kk]) : 0.f;
+  if (kk < slab) {
+#pragma unroll
+    for (int q = 0; q < TT / 4; ++q)
+      *reinterpret_cast<float4*>(xs + kk * (TT + 4) + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                                                                          v[4 * q + 3]);
+  }
+}
+
+template <int TT>
 __global__ void __launch_bounds__(256) router_partial_kernel(
     const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, float* __restrict__ part,
     int T, int d, int E, int kc_len) {
-  __shared__ float xs[kTT][kSlab];
+  constexpr int XS = TT + 4;  // padded row of the transposed x slab
+  __shared__ __align__(16) float xs[kSlab][XS];
   const int kc = blockIdx.x;
-  const int t0 = blockIdx.y * kTT;
+  const int t0 = blockIdx.y * TT;
   const int e = threadIdx.x;
-  const int nt = min(kTT, T - t0);
-  float acc[kTT];
+  const int nt = min(TT, T - t0);
+  float acc[TT];
 #pragma unroll
-  for (int t = 0; t < kTT; ++t) acc[t] = 0.f;
+  for (int t = 0; t < TT; ++t) acc[t] = 0.f;
   const int kbeg = kc * kc_len;
   for (int k0 = kbeg; k0 < kbeg + kc_len; k0 += kSlab) {
     const int slab = min(kSlab, kbeg + kc_len - k0);
     __syncthreads();
-    for (int i = threadIdx.x; i < kTT * slab; i += blockDim.x) {
-      const int t = i / slab, kk = i % slab;
-      xs[t][kk] = (t < nt) ? __bfloat162float(x[(size_t)(t0 + t) * d + k0 + kk]) : 0.f;
-    }
+    stage_x_slab<TT>(x, d, t0, nt, k0, slab, &xs[0][0]);
     __syncthreads();
     if (e < E) {
       const float* wp = wr + (size_t)k0 * E + e;
-#pragma unroll 8
+#pragma unroll 4
       for (int kk = 0; kk < slab; ++kk) {
         const float wv = __ldg(wp + (size_t)kk * E);
+        const float4* xv = reinterpret_cast<const float4*>(&xs[kk][0]);
 #pragma unroll
-        for (int t = 0; t < kTT; ++t) acc[t] = fmaf(xs[t][kk], wv, acc[t]);
+        for (int q = 0; q < TT / 4; ++q) {
+          const float4 v = xv[q];
+          acc[4 * q + 0] = fmaf(v.x, wv, acc[4 * q + 0]);
+          acc[4 * q + 1] = fmaf(v.y, wv, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(v.z, wv, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(v.w, wv, acc[4 * q + 3]);
+        }
       }
     }
   }
   if (e < E) {
-    for (int t = 0; t < nt; ++t) part[((size_t)kc * T + t0 + t) * E + e] = acc[t];
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+      if (t < nt) part[((size_t)kc * T + t0 + t) * E + e] = acc[t];
+  }
+}
+
+// Same partial sums as router_partial_kernel (same k order, so bit-identical),
+// for large token tiles: W_r is streamed through shared memory in 32-row
+// sub-slabs by a 4-deep cp.async ring, so each thread has a whole CTA's worth
+// of W_r bytes in flight instead of a few loads of its own.
+constexpr int kWRows = 32;
+constexpr int kWStages = 4;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(sa), "l"(gmem) : "memory");
+}
+
+template <int TT>
+constexpr size_t staged_smem_bytes() {
+  return (size_t)kSlab * (TT + 4) * 4 + (size_t)kWStages * kWRows * 256 * 4;
+}
+
+template <int TT>
+__global__ void __launch_bounds__(256, 1) router_partial_staged_kernel(
+    const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, float* __restrict__ part,
+    int T, int d, int E, int kc_len) {
+  constexpr int XS = TT + 4;
+  extern __shared__ __align__(16) float rsm[];
+  float* xs = rsm;                      // [kSlab][XS]
+  float* ws = rsm + kSlab * XS;         // [kWStages][kWRows][256]
+  const int kc = blockIdx.x;
+  const int t0 = blockIdx.y * TT;
+  const int e = threadIdx.x;
+  const int nt = min(TT, T - t0);
+  const int kbeg = kc * kc_len;
+  const int nsub = kc_len / kWRows;
+  const int e4 = E / 4;
+  auto issue = [&](int sub) {
+    if (sub < nsub) {
+      const float* src = wr + (size_t)(kbeg + sub * kWRows) * E;
+      float* dst = ws + (sub % kWStages) * kWRows * 256;
+      for (int i = threadIdx.x; i < kWRows * e4; i += blockDim.x) {
+        const int r = i / e4, q = i % e4;
+        cp_async16(dst + r * 256 + 4 * q, src + (size_t)r * E + 4 * q);
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  float acc[TT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+  for (int s = 0; s < kWStages - 1; ++s) issue(s);
+  for (int sub = 0; sub < nsub; ++sub) {
+    __syncthreads();  // compute(sub - 1) is done: its W stage and (on a slab edge) xs are free
+    const int kin = (sub * kWRows) % kSlab;
+    if (kin == 0) {
+      const int k0 = kbeg + sub * kWRows;
+      const int slab = min(kSlab, kbeg + kc_len - k0);
+      stage_x_slab<TT>(x, d, t0, nt, k0, slab, xs);
+    }
+    issue(sub + kWStages - 1);
+    asm volatile("cp.async.wait_group %0;" :: "n"(kWStages - 1) : "memory");
+    __syncthreads();
+    if (e < E) {
+      const float* wrow = ws + (sub % kWStages) * kWRows * 256 + e;
+#pragma unroll 4
+      for (int r = 0; r < kWRows; ++r) {
+        const float wv = wrow[r * 256];
+        const float4* xv = reinterpret_cast<const float4*>(xs + (kin + r) * XS);
+#pragma unroll
+        for (int q = 0; q < TT / 4; ++q) {
+          const float4 v = xv[q];
+          acc[4 * q + 0] = fmaf(v.x, wv, acc[4 * q + 0]);
+          acc[4 * q + 1] = fmaf(v.y, wv, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(v.z, wv, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(v.w, wv, acc[4 * q + 3]);
+        }
+      }
+    }
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  if (e < E) {
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+      if (t < nt) part[((size_t)kc * T + t0 + t) * E + e] = acc[t];
   }
 }
 
@@ -69,36 +180,34 @@ __device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
 __global__ void __launch_bounds__(256) router_topk_kernel(
     const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
     int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (t >= T) return;
+  __shared__ float lg[256];
+  const int t = blockIdx.x;
+  const int e = threadIdx.x;
+  if (e < E) {
+    // partial sums in a fixed order; 16 independent loads in flight per step
+    float v = 0.f;
+    for (int kc0 = 0; kc0 < nkc; kc0 += 16) {
+      float pv[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        pv[q] = (kc0 + q < nkc) ? __ldg(part + ((size_t)(kc0 + q) * T + t) * E + e) : 0.f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (kc0 + q < nkc) v += pv[q];
+    }
+    if (has_bias) v += bias[e];
+    lg[e] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
   float v[8];
   bool taken[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int e = lane + 32 * i;
-    taken[i] = e >= E;
-    v[i] = 0.f;
-  }
-  // partial sums in a fixed order; 8 independent loads in flight per step
-  for (int kc0 = 0; kc0 < nkc; kc0 += 8) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) {
-        float pv[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          pv[q] = (kc0 + q < nkc) ? __ldg(part + ((size_t)(kc0 + q) * T + t) * E + e) : 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[i] += pv[q];
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E && has_bias) v[i] += bias[e];
+    const int ee = lane + 32 * i;
+    taken[i] = ee >= E;
+    v[i] = ee < E ? lg[ee] : 0.f;
   }
   float sel_v[8];
   int sel_e[8];
@@ -107,8 +216,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
     int be = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (!taken[i] && (be == 0x7fffffff || beats(v[i], e, bv, be))) { bv = v[i]; be = e; }
+      const int ee = lane + 32 * i;
+      if (!taken[i] && (be == 0x7fffffff || beats(v[i], ee, bv, be))) { bv = v[i]; be = ee; }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -127,12 +236,33 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
     float z[8], sum = 0.f;
     for (int j = 0; j < K; ++j) { z[j] = __expf(sel_v[j] - m); sum += z[j]; }
     for (int j = 0; j < K; ++j) {
-      int e = sel_e[j];
-      if (e < 0 || e >= E) { latch_status(status, MOE_ERR_DEVICE_CHECK); e = 0; }
-      idx[(size_t)t * K + j] = e;
+      int ee = sel_e[j];
+      if (ee < 0 || ee >= E) { latch_status(status, MOE_ERR_DEVICE_CHECK); ee = 0; }
+      idx[(size_t)t * K + j] = ee;
       wout[(size_t)t * K + j] = z[j] / sum;
     }
   }
+}
+
+int router_tile(int T) { return T >= 256 ? 32 : 8; }
+
+cudaError_t launch_router_kernels(const __nv_bfloat16* x, int T, const float* wr, const float* bias,
+                                  int has_bias, int d, int E, int K, float* part, int32_t* idx, float* w,
+                                  int* status, cudaStream_t s) {
+  const int nkc = router_chunks(d, T);
+  const int tt = router_tile(T);
+  const dim3 g1(nkc, (T + tt - 1) / tt);
+  const bool staged = E % 4 == 0 && (reinterpret_cast<uintptr_t>(wr) & 15u) == 0 && (d / nkc) % kWRows == 0;
+  if (tt == 32 && staged)
+    router_partial_staged_kernel<32><<<g1, 256, staged_smem_bytes<32>(), s>>>(x, wr, part, T, d, E, d / nkc);
+  else if (tt == 32)
+    router_partial_kernel<32><<<g1, 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
+  else
+    router_partial_kernel<8><<<g1, 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  router_topk_kernel<<<T, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status);
+  return cudaGetLastError();
 }
 
 // Scratch of the allocation-free router entry point: the split-K partial
@@ -147,27 +277,31 @@ std::atomic<float*> g_static_partials_addr[kMaxCachedDevices];
 
 }  // namespace
 
+cudaError_t prepare_router_kernels() {
+  return cudaFuncSetAttribute(router_partial_staged_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)staged_smem_bytes<32>());
+}
+
+// K chunks of the split-K router for T tokens: about 256 CTAs, at most 64
+// chunks and at least 32 rows per chunk, a power of two that divides d, and
+// never more than 4096 / T chunks (so the partials hold at most
+// max(T, 4096) x E values).
 int router_chunks(int d, int T) {
-  const int tiles = (T + kTT - 1) / kTT;
-  int kc = 512 / (tiles > 0 ? tiles : 1);
+  const int tt = router_tile(T);
+  const int tiles = (T + tt - 1) / tt;
+  int kc = 256 / (tiles > 0 ? tiles : 1);
   if (kc > 64) kc = 64;
   if (kc > d / 32) kc = d / 32;
+  if (T > 0 && kc > 4096 / T) kc = 4096 / T;
   if (kc < 1) kc = 1;
-  int p = 1;  // power of two that divides d
+  int p = 1;
   while (p * 2 <= kc) p *= 2;
   return p;
 }
 
 cudaError_t launch_router(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s) {
-  const int d = c->cfg.d_model, E = c->cfg.n_experts;
-  const int nkc = router_chunks(d, T);
-  dim3 g1(nkc, (T + kTT - 1) / kTT);
-  router_partial_kernel<<<g1, 256, 0, s>>>(x, c->router, c->router_partial, T, d, E, d / nkc);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  router_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(c->router_partial, c->bias, c->has_bias, T, E,
-                                                 c->cfg.top_k, nkc, c->r.idx, c->r.w, c->status);
-  return cudaGetLastError();
+  return launch_router_kernels(x, T, c->router, c->bias, c->has_bias, c->cfg.d_model, c->cfg.n_experts,
+                               c->cfg.top_k, c->router_partial, c->r.idx, c->r.w, c->status, s);
 }
 
 size_t router_static_capacity() { return kStaticPartials; }
@@ -182,14 +316,10 @@ cudaError_t launch_router_static(const __nv_bfloat16* x, int T, const float* wr,
   if (!part) {
     err = cudaGetSymbolAddress((void**)&part, g_static_partials);
     if (err != cudaSuccess) return err;
+    if ((err = prepare_router_kernels()) != cudaSuccess) return err;
     if (dev < kMaxCachedDevices) g_static_partials_addr[dev].store(part, std::memory_order_release);
   }
-  const int nkc = router_chunks(d, T);
-  router_partial_kernel<<<dim3(nkc, (T + kTT - 1) / kTT), 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  router_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, bias, bias != nullptr, T, E, K, nkc, idx, w,
-                                                 nullptr);
-  return cudaGetLastError();
+  return launch_router_kernels(x, T, wr, bias, bias != nullptr, d, E, K, part, idx, w, nullptr, s);
 }
 
 }  // namespace nvmoe
