@@ -12,7 +12,9 @@
 //   C. warp 0 scans the per-expert totals into offsets and compacts the
 //      active experts (count > 0), shared experts appended;
 //   D. every pair lands at offsets[e] + prefix[chunk][e] + rank.
-// All sums are integer, so the result is exact and deterministic.
+// All sums are integer, so the result is exact and deterministic.  When they
+// fit (up to a few thousand tokens), the per-chunk counts, ranks and chosen
+// experts stay in shared memory; otherwise they go through global scratch.
 #include "internal.h"
 
 namespace nvmoe {
@@ -22,14 +24,20 @@ namespace {
 constexpr int kBucketThreads = 1024;
 constexpr int kMaxE = 256;
 
+template <bool kSmem>
 __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T, int k, int E,
                                                                 int S, int* status) {
+  extern __shared__ __align__(16) uint8_t bsm[];
+  // shared-memory variant: pre [nchunks][E] uint16, then chosen expert and rank per pair (uint8)
+  uint16_t* pre = reinterpret_cast<uint16_t*>(bsm);
   __shared__ uint32_t mask[kBucketThreads / 32][kMaxE];
   __shared__ int cnt[kMaxE];
   __shared__ int off[kMaxE + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int nchunks = (T + 31) / 32;
+  uint8_t* ej_s = bsm + (size_t)nchunks * E * 2;
+  uint8_t* rank_s = ej_s + (size_t)T * k;
 
   // A. per-chunk ranks and counts
   for (int c = warp; c < nchunks; c += nwarps) {
@@ -49,9 +57,21 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T
     __syncwarp();
     if (valid) {
       const uint32_t lower = (1u << lane) - 1u;
-      for (int j = 0; j < k; ++j) r.rank[(size_t)t * k + j] = __popc(mask[warp][ej[j]] & lower);
+      for (int j = 0; j < k; ++j) {
+        const int rk = __popc(mask[warp][ej[j]] & lower);
+        if (kSmem) {
+          rank_s[(size_t)t * k + j] = static_cast<uint8_t>(rk);
+          ej_s[(size_t)t * k + j] = static_cast<uint8_t>(ej[j]);
+        } else {
+          r.rank[(size_t)t * k + j] = rk;
+        }
+      }
     }
-    for (int e = lane; e < E; e += 32) r.chunk_cnt[(size_t)c * E + e] = __popc(mask[warp][e]);
+    for (int e = lane; e < E; e += 32) {
+      const int v = __popc(mask[warp][e]);
+      if (kSmem) pre[(size_t)c * E + e] = static_cast<uint16_t>(v);
+      else r.chunk_cnt[(size_t)c * E + e] = v;
+    }
     __syncwarp();
   }
   __syncthreads();
@@ -60,10 +80,18 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T
   if (threadIdx.x < E) {
     const int e = threadIdx.x;
     int run = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = r.chunk_cnt[(size_t)c * E + e];
-      r.chunk_cnt[(size_t)c * E + e] = run;
-      run += v;
+    if (kSmem) {
+      for (int c = 0; c < nchunks; ++c) {
+        const int v = pre[(size_t)c * E + e];
+        pre[(size_t)c * E + e] = static_cast<uint16_t>(run);
+        run += v;
+      }
+    } else {
+      for (int c = 0; c < nchunks; ++c) {
+        const int v = r.chunk_cnt[(size_t)c * E + e];
+        r.chunk_cnt[(size_t)c * E + e] = run;
+        run += v;
+      }
     }
     cnt[e] = run;
   }
@@ -126,9 +154,15 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T
   // D. stable scatter
   for (int s = threadIdx.x; s < T * k; s += blockDim.x) {
     const int t = s / k;
-    int e = r.idx[s];
-    if (e < 0 || e >= E) e = 0;
-    const int p = off[e] + r.chunk_cnt[(size_t)(t >> 5) * E + e] + r.rank[s];
+    int p;
+    if (kSmem) {
+      const int e = ej_s[s];
+      p = off[e] + pre[(size_t)(t >> 5) * E + e] + rank_s[s];
+    } else {
+      int e = r.idx[s];
+      if (e < 0 || e >= E) e = 0;
+      p = off[e] + r.chunk_cnt[(size_t)(t >> 5) * E + e] + r.rank[s];
+    }
     r.perm[p] = s;
     r.slot_pos[s] = p;
     r.pos_tok[p] = t;
@@ -138,9 +172,21 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T
 
 }  // namespace
 
+size_t bucket_smem_bytes(int T, int k, int E) { return (size_t)((T + 31) / 32) * E * 2 + (size_t)2 * T * k; }
+
+constexpr size_t kBucketSmemMax = 180 * 1024;
+
+cudaError_t prepare_bucket_kernel() {
+  return cudaFuncSetAttribute(bucket_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBucketSmemMax);
+}
+
 cudaError_t launch_bucket(const moe_ctx* c, int T, cudaStream_t s) {
-  bucket_kernel<<<1, kBucketThreads, 0, s>>>(c->r, T, c->cfg.top_k, c->cfg.n_experts,
-                                              c->cfg.n_shared, c->status);
+  const int k = c->cfg.top_k, E = c->cfg.n_experts, S = c->cfg.n_shared;
+  const size_t smem = bucket_smem_bytes(T, k, E);
+  if (smem <= kBucketSmemMax)
+    bucket_kernel<true><<<1, kBucketThreads, smem, s>>>(c->r, T, k, E, S, c->status);
+  else
+    bucket_kernel<false><<<1, kBucketThreads, 0, s>>>(c->r, T, k, E, S, c->status);
   return cudaGetLastError();
 }
 

@@ -579,13 +579,25 @@ static size_t down_smem(const moe_config& c) {
   return (size_t)NS * kRD * (F / 2 + F / 16) + (size_t)NS * (F + F / 8) * sizeof(float) + 64;
 }
 
+// The three kernels of a token overlap through PDL only if an SM can hold an
+// experts CTA and a down CTA (and a router CTA) at once, so every one of them
+// asks for the largest shared-memory carveout: with a carveout sized for one
+// kernel alone, the next kernel's CTAs would wait for the SM to drain.
+template <typename K>
+cudaError_t max_carveout(K kern) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t prepare_b1_kernels(const moe_ctx* c) {
   if (!c->b1_enabled) return cudaSuccess;
-  cudaError_t e = c->cfg.d_model == 2048
-                      ? cudaFuncSetAttribute(experts_b1_kernel<2048>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool d2k = c->cfg.d_model == 2048;
+  cudaError_t e = d2k ? cudaFuncSetAttribute(experts_b1_kernel<2048>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)c->b1_smem)
                       : cudaFuncSetAttribute(experts_b1_kernel<4096>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)c->b1_smem);
+  if (e == cudaSuccess) e = d2k ? max_carveout(experts_b1_kernel<2048>) : max_carveout(experts_b1_kernel<4096>);
+  if (e == cudaSuccess) e = d2k ? max_carveout(router_b1_kernel<2048>) : max_carveout(router_b1_kernel<4096>);
+  if (e == cudaSuccess) e = max_carveout(down_b1_kernel<512>);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(down_b1_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)down_smem(c->cfg));

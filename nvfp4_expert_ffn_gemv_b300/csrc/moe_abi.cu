@@ -94,6 +94,8 @@ size_t carve(moe_ctx* x, uint8_t* base) {
     const size_t rows = prefill_max_rows(c);
     x->pf_sfa_gu = cv.take<uint8_t>(base, n * 2 * f * d / 16);
     x->pf_sfa_dn = cv.take<uint8_t>(base, n * d * f / 16);
+    x->pf_xq_tok = cv.take<uint8_t>(base, T * d / 2);
+    x->pf_xsf_tok = cv.take<uint8_t>(base, T * d / 16);
     x->pf_xq = cv.take<uint8_t>(base, rows * d / 2);
     x->pf_xsf = cv.take<uint8_t>(base, rows * d / 16);
     x->pf_hq = cv.take<uint8_t>(base, rows * f / 2);
@@ -259,6 +261,7 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
   }
   if (e == cudaSuccess) e = cudaMemset(x->status, 0, sizeof(int));
   if (e == cudaSuccess) e = prepare_router_kernels();
+  if (e == cudaSuccess) e = prepare_bucket_kernel();
   if (e == cudaSuccess) e = prepare_decode_kernels(x);
   if (e == cudaSuccess && x->mma_enabled) e = prepare_mma_decode(x);
   if (e == cudaSuccess && x->pf_enabled) {
@@ -426,7 +429,7 @@ moe_status moe_get_device_status(moe_ctx* x) {
 int moe_kernels_per_forward(moe_ctx* x, int T, int prefill) {
   if (!x || T <= 0) return 0;
   if (!prefill && T == 1 && x->b1_enabled) return 3;
-  if (prefill) return 8;   // router x2, bucket, plan, quantise x, GEMM x2, combine
+  if (prefill) return 9;   // router x2, bucket, plan, quantise x, gather x, GEMM x2, combine
   if (x->mma_enabled) return 7;   // router x2, bucket, x prescale, gate/up, down, combine
   return 6;
 }

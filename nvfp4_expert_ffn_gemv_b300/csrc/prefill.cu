@@ -120,35 +120,22 @@ __device__ __forceinline__ size_t sf_atom_offset(int p, int b, int ksteps) {
   return ((size_t)(p >> 7) * ksteps + (b >> 2)) * 512 + (p & 31) * 16 + ((p >> 5) & 3) * 4 + (b & 3);
 }
 
-// x rows -> NVFP4 in padded position order; one warp per padded row, each lane
-// four 16-element blocks (d = 2048) or fewer.
-__global__ void __launch_bounds__(256) quant_x_kernel(Routing r, const __nv_bfloat16* __restrict__ x, int d,
-                                                      uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-                                                      int max_rows) {
+// x -> NVFP4, once per token (one warp per token, canonical layout).
+__global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int d,
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = blockIdx.x * 8 + warp;
-  const int na = *r.n_active;
-  const int total = r.act_ppos[na];
-  if (p >= total || p >= max_rows) return;
-  const int a = find_seg(r.act_ppos, na, p);
-  const int i = p - r.act_ppos[a];
-  const bool real = i < r.act_n[a];
-  const int t = real ? r.pos_tok[r.act_pos[a] + i] : 0;
-  const int nblk = d / 16, ksteps = d / 64;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const int nblk = d / 16;
   for (int b = lane; b < nblk; b += 32) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + b * 16);
+    const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
     float v[16];
-    if (real) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + b * 16);
-      const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-      const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        v[2 * q] = __uint_as_float(w[q] << 16);
-        v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
-      }
-    } else {
-#pragma unroll
-      for (int q = 0; q < 16; ++q) v[q] = 0.f;
+    for (int q = 0; q < 8; ++q) {
+      v[2 * q] = __uint_as_float(w[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
     }
     float amax = 0.f;
 #pragma unroll
@@ -163,9 +150,33 @@ __global__ void __launch_bounds__(256) quant_x_kernel(Routing r, const __nv_bflo
         hi |= q_e2m1x2(__fdiv_rn(v[8 + 2 * q], dq), __fdiv_rn(v[8 + 2 * q + 1], dq)) << (8 * q);
       }
     }
-    reinterpret_cast<uint2*>(codes + (size_t)p * (d / 2))[b] = make_uint2(lo, hi);
-    sf[sf_atom_offset(p, b, ksteps)] = static_cast<uint8_t>(s);
+    reinterpret_cast<uint2*>(codes + (size_t)t * (d / 2))[b] = make_uint2(lo, hi);
+    sc[(size_t)t * nblk + b] = static_cast<uint8_t>(s);
   }
+}
+
+// Quantised token rows -> padded position order, scales into the MMA's
+// scale-factor atoms (one warp per padded row; padding rows are zero).
+__global__ void __launch_bounds__(256) gather_x_kernel(Routing r, const uint8_t* __restrict__ tq,
+                                                       const uint8_t* __restrict__ tsc, int d,
+                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                       int max_rows) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p = blockIdx.x * 8 + warp;
+  const int na = *r.n_active;
+  const int total = r.act_ppos[na];
+  if (p >= total || p >= max_rows) return;
+  const int a = find_seg(r.act_ppos, na, p);
+  const int i = p - r.act_ppos[a];
+  const bool real = i < r.act_n[a];
+  const int t = real ? r.pos_tok[r.act_pos[a] + i] : 0;
+  const int ksteps = d / 64;
+  const uint4* src = reinterpret_cast<const uint4*>(tq + (size_t)t * (d / 2));
+  uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)p * (d / 2));
+  for (int q = lane; q < d / 32; q += 32) dst[q] = real ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(tsc + (size_t)t * (d / 16));
+  for (int ks = lane; ks < ksteps; ks += 32)
+    *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(p, 4 * ks, ksteps)) = real ? __ldg(ssrc + ks) : 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -189,23 +200,51 @@ struct GemmArgs {
   int* status;
 };
 
+// Active-expert tables copied to shared memory once per CTA, so that mapping a
+// tile index to its expert costs shared-memory reads only (a binary search
+// over global memory would put several dependent L2 round trips in front of
+// every TMA issue).
+constexpr int kMaxActive = 256 + 2 + 1;
+struct ActTables {
+  int ppos[kMaxActive];   // padded first row, total last
+  int e[kMaxActive];
+  int n[kMaxActive];
+  int pos[kMaxActive];
+};
+
 // unit u -> (128-token block, 128-row weight tile)
 struct UnitInfo {
   int a, e, p0, nt, ntile;
 };
 
-__device__ __forceinline__ UnitInfo decode_unit(const GemmArgs& g, int u, int ntiles, int na) {
+__device__ __forceinline__ UnitInfo decode_unit(const ActTables& t, int u, int ntiles, int na) {
   UnitInfo ui;
   const int tb = u / ntiles;
   ui.ntile = u % ntiles;
   ui.p0 = tb * kBM;
-  ui.a = find_seg(g.r.act_ppos, na, ui.p0);
-  ui.e = g.r.act_e[ui.a];
-  ui.nt = min(kBM, g.r.act_n[ui.a] - (ui.p0 - g.r.act_ppos[ui.a]));   // real tokens in the block
+  int lo = 0, hi = na - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (t.ppos[mid] <= ui.p0) lo = mid; else hi = mid - 1;
+  }
+  ui.a = lo;
+  ui.e = t.e[lo];
+  ui.nt = min(kBM, t.n[lo] - (ui.p0 - t.ppos[lo]));   // real tokens in the block
   return ui;
 }
 
-__device__ __forceinline__ float silu_acc(float z) { return z / (1.0f + expf(-z)); }
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// E2M1 code of v / dq, rounded to nearest with ties to the even code, decided
+// without dividing: |v| is compared with each rounding midpoint times dq.
+// Midpoints have at most 3 significant bits and dq (an E4M3 value) at most 4,
+// so every product is exact and the comparison is that of the exact quotient.
+__device__ __forceinline__ uint32_t e2m1_by_compare(float v, float dq) {
+  const float a = fabsf(v);
+  const uint32_t c = (a > 0.25f * dq) + (a >= 0.75f * dq) + (a > 1.25f * dq) + (a >= 1.75f * dq) +
+                     (a > 2.5f * dq) + (a >= 3.5f * dq) + (a > 5.0f * dq);
+  return (v < 0.f && c != 0u) ? (c | 8u) : c;
+}
 
 // NVFP4 (scale 1) of 16 consecutive fp32 values held by one thread -> 8 code bytes, one scale byte
 __device__ __forceinline__ uint32_t quant16(const float* v, uint2& codes) {
@@ -217,9 +256,9 @@ __device__ __forceinline__ uint32_t quant16(const float* v, uint2& codes) {
   uint32_t lo = 0, hi = 0;
   if (dq > 0.f) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      lo |= q_e2m1x2(__fdiv_rn(v[2 * q], dq), __fdiv_rn(v[2 * q + 1], dq)) << (8 * q);
-      hi |= q_e2m1x2(__fdiv_rn(v[8 + 2 * q], dq), __fdiv_rn(v[8 + 2 * q + 1], dq)) << (8 * q);
+    for (int q = 0; q < 8; ++q) {
+      lo |= e2m1_by_compare(v[q], dq) << (4 * q);
+      hi |= e2m1_by_compare(v[8 + q], dq) << (4 * q);
     }
   }
   codes = make_uint2(lo, hi);
@@ -233,10 +272,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], dfull_bar[2], dempty_bar[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_flag;
+  __shared__ ActTables tab;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int na = *g.r.n_active;
+  for (int i = threadIdx.x; i <= na; i += blockDim.x) {
+    tab.ppos[i] = g.r.act_ppos[i];
+    if (i < na) {
+      tab.e[i] = g.r.act_e[i];
+      tab.n[i] = g.r.act_n[i];
+      tab.pos[i] = g.r.act_pos[i];
+    }
+  }
   const int ntiles = g.M / kBN, ksteps = g.K / 64, kstages = g.K / kStageK;
-  const int U = (g.r.act_ppos[na] / kBM) * ntiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -259,6 +306,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  const int U = (tab.ppos[na] / kBM) * ntiles;
 
   auto bounded_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (abort_flag) return false;
@@ -274,7 +322,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
-        const UnitInfo ui = decode_unit(g, u, ntiles, na);
+        const UnitInfo ui = decode_unit(tab, u, ntiles, na);
         const int brow = ui.e * g.M + ui.ntile * kBN;
         const uint8_t* sfa = g.sfa + (size_t)(ui.p0 / kBM) * ksteps * 512;
         const uint8_t* sfb = g.sfb + ((size_t)ui.e * ntiles + ui.ntile) * ksteps * 512;
@@ -333,7 +381,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // Every epilogue warp runs the same units and never leaves the loop early
     // (a failed wait only skips the work), so all four always arrive.
     for (int u = blockIdx.x; u < U; u += gridDim.x, ++i) {
-      const UnitInfo ui = decode_unit(g, u, ntiles, na);
+      const UnitInfo ui = decode_unit(tab, u, ntiles, na);
       const int buf = i & 1;
       const bool ok = bounded_wait(&dfull_bar[buf], (i >> 1) & 1);
       tc_fence_after();
@@ -357,7 +405,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           float hv[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            hv[j] = silu_acc(__uint_as_float(gv[j]) * tg) * (__uint_as_float(uv[j]) * tu);
+            hv[j] = silu_fast(__uint_as_float(gv[j]) * tg) * (__uint_as_float(uv[j]) * tu);
           uint2 c0, c1;
           const uint32_t s0 = quant16(hv, c0), s1 = quant16(hv + 16, c1);
           sc4 |= (s0 | (s1 << 8)) << (16 * half);
@@ -368,10 +416,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // the 4 block scales of these 64 hidden units are one k-step of the down GEMM: 4 adjacent bytes
         if (ok) *reinterpret_cast<uint32_t*>(g.hq_sf + sf_atom_offset(p, ui.ntile * 4, g.f / 64)) = sc4;
       } else {
-        const int i_tok = p - g.r.act_ppos[ui.a];   // index among the expert's tokens
+        const int i_tok = p - tab.ppos[ui.a];   // index among the expert's tokens
         const bool real = ok && m < ui.nt;
         const float td = ts[2];
-        float* dst = g.yexp + (size_t)(g.r.act_pos[ui.a] + i_tok) * g.d + ui.ntile * kBN;
+        float* dst = g.yexp + (size_t)(tab.pos[ui.a] + i_tok) * g.d + ui.ntile * kBN;
 #pragma unroll 1
         for (int c0 = 0; c0 < kBN; c0 += 32) {
           uint32_t v[32];
@@ -479,7 +527,9 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   prefill_plan_kernel<<<1, 32, 0, s>>>(c->r);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  quant_x_kernel<<<(rows + 7) / 8, 256, 0, s>>>(c->r, x, d, c->pf_xq, c->pf_xsf, rows);
+  quant_tokens_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, d, c->pf_xq_tok, c->pf_xsf_tok);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  gather_x_kernel<<<(rows + 7) / 8, 256, 0, s>>>(c->r, c->pf_xq_tok, c->pf_xsf_tok, d, c->pf_xq, c->pf_xsf, rows);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   GemmArgs g{};
   g.r = c->r;
@@ -505,7 +555,6 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   g.mode = 1;
   g.yexp = c->yexp;
   moe_gemm_kernel<<<c->sm_count, kGemmThreads, kSmemGemm, s>>>(c->pf_tm[3], c->pf_tm[1], g);
-  (void)T;
   return cudaGetLastError();
 }
 

@@ -26,21 +26,24 @@ namespace {
 constexpr int kSlab = 256;  // rows of W_r staged per x slab
 
 // Transposed x slab xs[kk][t] (row stride TT + 4) for k0 <= k < k0 + slab:
-// thread kk (blockDim == kSlab) loads its TT values at once, so all of a
-// thread's L2 loads are in flight together.
-template <int TT>
+// thread i loads the TT / NPART values t = (i / kSlab) * TT / NPART + .. of
+// row kk = i % kSlab at once, so all of a thread's L2 loads are in flight
+// together (blockDim == kSlab * NPART).
+template <int TT, int NPART>
 __device__ __forceinline__ void stage_x_slab(const __nv_bfloat16* __restrict__ x, int d, int t0, int nt, int k0,
                                              int slab, float* xs) {
-  const int kk = threadIdx.x;
-  float v[TT];
+  constexpr int TP = TT / NPART;
+  const int kk = threadIdx.x % kSlab;
+  const int tb = (threadIdx.x / kSlab) * TP;
+  float v[TP];
 #pragma unroll
-  for (int t = 0; t < TT; ++t)
-    v[t] = (t < nt && kk < slab) ? __bfloat162float(x[(size_t)(t0 + t) * d + k0 + kk]) : 0.f;
+  for (int t = 0; t < TP; ++t)
+    v[t] = (tb + t < nt && kk < slab) ? __bfloat162float(x[(size_t)(t0 + tb + t) * d + k0 + kk]) : 0.f;
   if (kk < slab) {
 #pragma unroll
-    for (int q = 0; q < TT / 4; ++q)
-      *reinterpret_cast<float4*>(xs + kk * (TT + 4) + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2],
-                                                                          v[4 * q + 3]);
+    for (int q = 0; q < TP / 4; ++q)
+      *reinterpret_cast<float4*>(xs + kk * (TT + 4) + tb + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                                                                               v[4 * q + 3]);
   }
 }
 
@@ -61,7 +64,7 @@ __global__ void __launch_bounds__(256) router_partial_kernel(
   for (int k0 = kbeg; k0 < kbeg + kc_len; k0 += kSlab) {
     const int slab = min(kSlab, kbeg + kc_len - k0);
     __syncthreads();
-    stage_x_slab<TT>(x, d, t0, nt, k0, slab, &xs[0][0]);
+    stage_x_slab<TT, 1>(x, d, t0, nt, k0, slab, &xs[0][0]);
     __syncthreads();
     if (e < E) {
       const float* wp = wr + (size_t)k0 * E + e;
@@ -88,33 +91,36 @@ __global__ void __launch_bounds__(256) router_partial_kernel(
 }
 
 // Same partial sums as router_partial_kernel (same k order, so bit-identical),
-// for large token tiles: W_r is streamed through shared memory in 32-row
-// sub-slabs by a 4-deep cp.async ring, so each thread has a whole CTA's worth
-// of W_r bytes in flight instead of a few loads of its own.
+// for 32-token tiles: W_r is streamed through shared memory in 32-row
+// sub-slabs by a 4-deep cp.async ring, and each of 512 threads accumulates 4
+// experts x 4 tokens, so one k step costs it two 16-byte shared loads for 16
+// FMAs, with 16 warps per SM to hide their latency.
 constexpr int kWRows = 32;
 constexpr int kWStages = 4;
+constexpr int kStagedTT = 32;
+constexpr int kStagedThreads = 512;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(sa), "l"(gmem) : "memory");
 }
 
-template <int TT>
 constexpr size_t staged_smem_bytes() {
-  return (size_t)kSlab * (TT + 4) * 4 + (size_t)kWStages * kWRows * 256 * 4;
+  return (size_t)kSlab * (kStagedTT + 4) * 4 + (size_t)kWStages * kWRows * 256 * 4;
 }
 
-template <int TT>
-__global__ void __launch_bounds__(256, 1) router_partial_staged_kernel(
+__global__ void __launch_bounds__(kStagedThreads, 1) router_partial_staged_kernel(
     const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, float* __restrict__ part,
     int T, int d, int E, int kc_len) {
+  constexpr int TT = kStagedTT;
   constexpr int XS = TT + 4;
   extern __shared__ __align__(16) float rsm[];
   float* xs = rsm;                      // [kSlab][XS]
   float* ws = rsm + kSlab * XS;         // [kWStages][kWRows][256]
   const int kc = blockIdx.x;
   const int t0 = blockIdx.y * TT;
-  const int e = threadIdx.x;
+  const int eq = threadIdx.x & 63;      // experts 4eq .. 4eq+3
+  const int tq = threadIdx.x >> 6;      // tokens 4tq .. 4tq+3 of the tile
   const int nt = min(TT, T - t0);
   const int kbeg = kc * kc_len;
   const int nsub = kc_len / kWRows;
@@ -130,43 +136,47 @@ __global__ void __launch_bounds__(256, 1) router_partial_staged_kernel(
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  float acc[TT];
+  float acc[4][4];
 #pragma unroll
-  for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   for (int s = 0; s < kWStages - 1; ++s) issue(s);
   for (int sub = 0; sub < nsub; ++sub) {
     __syncthreads();  // compute(sub - 1) is done: its W stage and (on a slab edge) xs are free
     const int kin = (sub * kWRows) % kSlab;
     if (kin == 0) {
       const int k0 = kbeg + sub * kWRows;
-      const int slab = min(kSlab, kbeg + kc_len - k0);
-      stage_x_slab<TT>(x, d, t0, nt, k0, slab, xs);
+      stage_x_slab<TT, kStagedThreads / kSlab>(x, d, t0, nt, k0, min(kSlab, kbeg + kc_len - k0), xs);
     }
     issue(sub + kWStages - 1);
     asm volatile("cp.async.wait_group %0;" :: "n"(kWStages - 1) : "memory");
     __syncthreads();
-    if (e < E) {
-      const float* wrow = ws + (sub % kWStages) * kWRows * 256 + e;
-#pragma unroll 4
+    if (4 * eq < E) {
+      const float* wrow = ws + (sub % kWStages) * kWRows * 256 + 4 * eq;
+      const float* xrow = xs + kin * XS + 4 * tq;
+#pragma unroll 8
       for (int r = 0; r < kWRows; ++r) {
-        const float wv = wrow[r * 256];
-        const float4* xv = reinterpret_cast<const float4*>(xs + (kin + r) * XS);
+        const float4 w = *reinterpret_cast<const float4*>(wrow + r * 256);
+        const float4 xa = *reinterpret_cast<const float4*>(xrow + r * XS);
+        const float wv[4] = {w.x, w.y, w.z, w.w};
+        const float xv[4] = {xa.x, xa.y, xa.z, xa.w};
 #pragma unroll
-        for (int q = 0; q < TT / 4; ++q) {
-          const float4 v = xv[q];
-          acc[4 * q + 0] = fmaf(v.x, wv, acc[4 * q + 0]);
-          acc[4 * q + 1] = fmaf(v.y, wv, acc[4 * q + 1]);
-          acc[4 * q + 2] = fmaf(v.z, wv, acc[4 * q + 2]);
-          acc[4 * q + 3] = fmaf(v.w, wv, acc[4 * q + 3]);
-        }
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[j], wv[i], acc[i][j]);
       }
     }
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
-  if (e < E) {
+  if (4 * eq < E) {
 #pragma unroll
-    for (int t = 0; t < TT; ++t)
-      if (t < nt) part[((size_t)kc * T + t0 + t) * E + e] = acc[t];
+    for (int j = 0; j < 4; ++j) {
+      const int t = 4 * tq + j;
+      if (t < nt)
+        *reinterpret_cast<float4*>(part + ((size_t)kc * T + t0 + t) * E + 4 * eq) =
+            make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+    }
   }
 }
 
@@ -177,38 +187,14 @@ __device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
   return a > b || (a == b && ia < ib);
 }
 
-__global__ void __launch_bounds__(256) router_topk_kernel(
-    const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
-    int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status) {
-  __shared__ float lg[256];
-  const int t = blockIdx.x;
-  const int e = threadIdx.x;
-  if (e < E) {
-    // partial sums in a fixed order; 16 independent loads in flight per step
-    float v = 0.f;
-    for (int kc0 = 0; kc0 < nkc; kc0 += 16) {
-      float pv[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        pv[q] = (kc0 + q < nkc) ? __ldg(part + ((size_t)(kc0 + q) * T + t) * E + e) : 0.f;
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        if (kc0 + q < nkc) v += pv[q];
-    }
-    if (has_bias) v += bias[e];
-    lg[e] = v;
-  }
-  __syncthreads();
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  float v[8];
+// k rounds of warp argmax over the (up to) 256 logits v[i] of expert lane + 32 i;
+// lane 0 writes idx and the renormalised softmax weights of token t.
+__device__ __forceinline__ void warp_select(const float (&v)[8], int E, int K, int t, int32_t* __restrict__ idx,
+                                            float* __restrict__ wout, int* status) {
+  const int lane = threadIdx.x & 31;
   bool taken[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int ee = lane + 32 * i;
-    taken[i] = ee >= E;
-    v[i] = ee < E ? lg[ee] : 0.f;
-  }
+  for (int i = 0; i < 8; ++i) taken[i] = lane + 32 * i >= E;
   float sel_v[8];
   int sel_e[8];
   for (int j = 0; j < K; ++j) {
@@ -244,6 +230,66 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
   }
 }
 
+// Many K chunks: one CTA per token; thread e sums its nkc partials in order.
+__global__ void __launch_bounds__(256) router_topk_kernel(
+    const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
+    int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status) {
+  __shared__ float lg[256];
+  const int t = blockIdx.x;
+  const int e = threadIdx.x;
+  if (e < E) {
+    // partial sums in a fixed order; 16 independent loads in flight per step
+    float v = 0.f;
+    for (int kc0 = 0; kc0 < nkc; kc0 += 16) {
+      float pv[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        pv[q] = (kc0 + q < nkc) ? __ldg(part + ((size_t)(kc0 + q) * T + t) * E + e) : 0.f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (kc0 + q < nkc) v += pv[q];
+    }
+    if (has_bias) v += bias[e];
+    lg[e] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int ee = threadIdx.x + 32 * i;
+    v[i] = ee < E ? lg[ee] : 0.f;
+  }
+  warp_select(v, E, K, t, idx, wout, status);
+}
+
+// Few K chunks (nkc <= 2): one warp per token, the same sums in the same order.
+__global__ void __launch_bounds__(256) router_topk_warp_kernel(
+    const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
+    int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  float p0[8], p1[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int ee = lane + 32 * i;
+    p0[i] = ee < E ? __ldg(part + (size_t)t * E + ee) : 0.f;
+    p1[i] = (ee < E && nkc > 1) ? __ldg(part + ((size_t)T + t) * E + ee) : 0.f;
+  }
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int ee = lane + 32 * i;
+    float s = 0.f;
+    s += p0[i];
+    if (nkc > 1) s += p1[i];
+    if (ee < E && has_bias) s += bias[ee];
+    v[i] = s;
+  }
+  warp_select(v, E, K, t, idx, wout, status);
+}
+
 int router_tile(int T) { return T >= 256 ? 32 : 8; }
 
 cudaError_t launch_router_kernels(const __nv_bfloat16* x, int T, const float* wr, const float* bias,
@@ -254,14 +300,17 @@ cudaError_t launch_router_kernels(const __nv_bfloat16* x, int T, const float* wr
   const dim3 g1(nkc, (T + tt - 1) / tt);
   const bool staged = E % 4 == 0 && (reinterpret_cast<uintptr_t>(wr) & 15u) == 0 && (d / nkc) % kWRows == 0;
   if (tt == 32 && staged)
-    router_partial_staged_kernel<32><<<g1, 256, staged_smem_bytes<32>(), s>>>(x, wr, part, T, d, E, d / nkc);
+    router_partial_staged_kernel<<<g1, kStagedThreads, staged_smem_bytes(), s>>>(x, wr, part, T, d, E, d / nkc);
   else if (tt == 32)
     router_partial_kernel<32><<<g1, 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
   else
     router_partial_kernel<8><<<g1, 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  router_topk_kernel<<<T, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status);
+  if (nkc <= 2)
+    router_topk_warp_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status);
+  else
+    router_topk_kernel<<<T, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status);
   return cudaGetLastError();
 }
 
@@ -278,8 +327,8 @@ std::atomic<float*> g_static_partials_addr[kMaxCachedDevices];
 }  // namespace
 
 cudaError_t prepare_router_kernels() {
-  return cudaFuncSetAttribute(router_partial_staged_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)staged_smem_bytes<32>());
+  return cudaFuncSetAttribute(router_partial_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)staged_smem_bytes());
 }
 
 // K chunks of the split-K router for T tokens: about 256 CTAs, at most 64
