@@ -4,15 +4,18 @@
 //   router_b1:  one warp per expert computes its fp32 logit x . W_r[:, e] (+bias)
 //               from the transposed router; the W_r row is loaded before the
 //               kernel waits on its predecessor, so it streams while the
-//               previous token (or layer) is still finishing.  The last CTA to
-//               finish (completion ticket) selects the top-k experts and their
-//               renormalised softmax weights.
+//               previous token (or layer) is still finishing.
+//   top-k:      not a kernel of its own: every CTA of the two kernels below
+//               selects the top-k experts and their renormalised softmax
+//               weights from the 256 logits with one warp (the same
+//               deterministic selection everywhere), so no CTA waits for a
+//               single selecting CTA.
 //   experts_b1: every CTA owns a slice of the shared expert's hidden rows and a
 //               slice of the 6 routed experts' hidden rows (a flat split of the
 //               6 x d_ff rows, so all CTAs move the same number of bytes).
 //               Before waiting it starts TMA bulk copies of its shared-expert
-//               rows; after the wait it reads the chosen experts and copies
-//               its routed rows.  Then, per hidden row j it owns:
+//               rows; after the wait it selects the experts and copies its
+//               routed rows.  Then, per hidden row j it owns:
 //                 g_j, u_j  = NVFP4 rows of W_gate / W_up . x
 //                 h_j       = silu(g_j) * u_j * w_slot * ts_down   -> global
 //   down_b1:    every CTA owns 16 output rows; it fetches those rows of
@@ -75,13 +78,6 @@ __device__ __forceinline__ int ld_once_s32(const int32_t* p) {
   int v;
   asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
-}
-
-// Completion ticket with acquire-release semantics at GPU scope.
-__device__ __forceinline__ unsigned ticket_add(unsigned* p) {
-  unsigned old;
-  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
-  return old;
 }
 
 // 2^k as a float for -126 <= k <= 127
@@ -151,18 +147,14 @@ __device__ __forceinline__ void warp_topk(const float* logits, int E, int k, int
 }
 
 // ---------------------------------------------------------------------------
-// router: logits, then the last CTA to finish selects the top-k
+// router: logits only
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(64) router_b1_kernel(const float* __restrict__ rt, const float* __restrict__ bias,
-                                                       int has_bias, const __nv_bfloat16* x, float* logits, int E,
-                                                       int k, unsigned* ticket, int32_t* idx_out, float* w_out) {
+                                                       int has_bias, const __nv_bfloat16* x, float* logits, int E) {
   constexpr int Q = D / 128;  // float4 of W_r per lane
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int e = blockIdx.x * 2 + w;
-  __shared__ int is_last;
-  __shared__ int top_idx[8];
-  __shared__ float top_w[8];
   float4 wv[Q];
   if (e < E) {
     const float4* p = reinterpret_cast<const float4*>(rt + (size_t)e * D);
@@ -185,26 +177,15 @@ __global__ void __launch_bounds__(64) router_b1_kernel(const float* __restrict__
     const float s = warp_sum(acc + acc2);
     if (l == 0) logits[e] = s + (has_bias ? bias[e] : 0.f);
   }
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = (ticket_add(ticket) == gridDim.x - 1);
-  __syncthreads();
-  if (!is_last || w != 0) return;
-  // last CTA: top-k with renormalised softmax weights
-  warp_topk(logits, E, k, top_idx, top_w);
-  __syncwarp();
-  if (l < k) {
-    idx_out[l] = top_idx[l];
-    w_out[l] = top_w[l];
-  }
-  if (l == 0) *ticket = 0u;
 }
 
 // ---------------------------------------------------------------------------
 // experts
 // ---------------------------------------------------------------------------
 struct B1Args {
-  const int32_t* idx_in;   // [k] chosen experts (router output)
-  const float* w_in;       // [k] their combine weights
+  const float* logits;     // [E] router output
+  int32_t* idx_out;        // [k] chosen experts (written by CTA 0, for inspection)
+  float* w_out;            // [k] their combine weights
   const __nv_bfloat16* x;
   const uint8_t* rows;     // [n_all][f][gate/up record]
   const float* tsc;
@@ -340,16 +321,21 @@ __global__ void __launch_bounds__(kB1Threads, 1) experts_b1_kernel(B1Args a) {
     }
     __syncwarp();
     issue_segment_copies<D>(a, seg, 0, nseg_sh, sm_gu, &bars[0]);
+    asm volatile("bar.arrive 1, 64;" ::: "memory");   // segment table handed to warp 1
   }
   griddep_wait();
 
-  if (warp == 0) {
-    // ---- routed experts chosen by the router's last CTA ----
-    if (lane < a.k) {
-      top_idx[lane] = ld_once_s32(a.idx_in + lane);
-      top_w[lane] = ld_once_f32(a.w_in + lane);
-    }
+  if (warp == 1) {
+    // ---- routed experts: top-k of the logits (the router grid has completed).
+    // Warp 1 rather than warp 0: the warp that issued the shared-expert bulk
+    // copies runs several times slower for a while afterwards. ----
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    warp_topk(a.logits, a.E, a.k, top_idx, top_w);
     __syncwarp();
+    if (c == 0 && lane < a.k) {
+      a.idx_out[lane] = top_idx[lane];
+      a.w_out[lane] = top_w[lane];
+    }
     if (lane == 0) {
       int row = n_rows;
       const int Nr = a.k * f;
@@ -359,9 +345,9 @@ __global__ void __launch_bounds__(kB1Threads, 1) experts_b1_kernel(B1Args a) {
     __syncwarp();
     issue_segment_copies<D>(a, seg, nseg_sh, nseg_all, sm_gu, &bars[1]);
   } else {
-    // ---- x -> shared memory (fp32), block max of |x| ----
+    // ---- x -> shared memory (fp32), block max of |x| (every warp but warp 1) ----
     float m = 0.f;
-    for (int i = threadIdx.x - 32; i < D / 8; i += kB1Threads - 32) {
+    for (int i = warp == 0 ? lane : threadIdx.x - 32; i < D / 8; i += kB1Threads - 32) {
       const uint4 t = __ldcg(reinterpret_cast<const uint4*>(a.x) + i);
       const uint32_t u[4] = {t.x, t.y, t.z, t.w};
       float4 lo, hi;
@@ -383,7 +369,8 @@ __global__ void __launch_bounds__(kB1Threads, 1) experts_b1_kernel(B1Args a) {
 
   // ---- x as prescaled f16 registers: lane l holds the columns of chunks l + 32q ----
   uint32_t mb = 0;
-  for (int w = 1; w < kB1Warps; ++w) mb = max(mb, wmax[w]);
+  for (int w = 0; w < kB1Warps; ++w)
+    if (w != 1) mb = max(mb, wmax[w]);
   const int ex = (int)((mb >> 23) & 0xFF) - 127;
   const int shift = (mb == 0u) ? 0 : max(-126, min(127, 14 - ex));
   uint32_t xh[CPL][16];
@@ -442,7 +429,7 @@ constexpr int kDThreads = 256;
 constexpr int kMaxSlots = 12;
 
 struct DnArgs {
-  const int32_t* idx_in;
+  const float* logits;
   const float* h;                 // [k + S][f]
   const __nv_bfloat16* x;
   __nv_bfloat16* y;
@@ -465,6 +452,8 @@ __global__ void __launch_bounds__(kDThreads) down_b1_kernel(DnArgs a) {
   constexpr int HP = F + F / 8;
   float* hs = reinterpret_cast<float*>(sc_scales + (size_t)NS * kRD * FS);  // [NS][HP]
   __shared__ __align__(8) uint64_t bar;
+  __shared__ int sel_idx[8];
+  __shared__ float sel_w[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.x * kRD;
 
@@ -473,11 +462,15 @@ __global__ void __launch_bounds__(kDThreads) down_b1_kernel(DnArgs a) {
     fence_barrier_init();
   }
   __syncthreads();
-  // routing is final (the router finished before the experts kernel passed its
-  // wait, and that kernel released this one afterwards): fetch W_down rows now
-  if (warp == 0) {
+  // the logits are final (the router finished before the experts kernel passed
+  // its wait, and that kernel released this one afterwards): select the same
+  // experts and fetch their W_down rows now (warp 1: warp 0 initialised the
+  // mbarrier and runs slowly for a while afterwards)
+  if (warp == 1) {
+    warp_topk(a.logits, a.E, a.k, sel_idx, sel_w);
+    __syncwarp();
     int e = 0;
-    if (lane < NS) e = lane < a.k ? ld_once_s32(a.idx_in + lane) : a.E + (lane - a.k);
+    if (lane < NS) e = lane < a.k ? sel_idx[lane] : a.E + (lane - a.k);
     if (lane == 0) mbar_arrive_expect_tx(&bar, (uint32_t)NS * kRD * (FB + FS));
     __syncwarp();
     if (lane < NS) {
@@ -608,16 +601,17 @@ cudaError_t launch_router_b1(const moe_ctx* c, const __nv_bfloat16* x, cudaStrea
   const dim3 grid((E + 1) / 2), block(64);
   if (c->cfg.d_model == 2048)
     return launch_pdl(router_b1_kernel<2048>, grid, block, 0, s, (const float*)c->router_t, (const float*)c->bias,
-                      c->has_bias, x, c->logits, E, c->cfg.top_k, c->ticket + 1, c->r.idx, c->r.w);
+                      c->has_bias, x, c->logits, E);
   return launch_pdl(router_b1_kernel<4096>, grid, block, 0, s, (const float*)c->router_t, (const float*)c->bias,
-                    c->has_bias, x, c->logits, E, c->cfg.top_k, c->ticket + 1, c->r.idx, c->r.w);
+                    c->has_bias, x, c->logits, E);
 }
 
 cudaError_t launch_experts_b1(const moe_ctx* c, const __nv_bfloat16* x, __nv_bfloat16* y, int residual,
                               cudaStream_t s) {
   B1Args a;
-  a.idx_in = c->r.idx;
-  a.w_in = c->r.w;
+  a.logits = c->logits;
+  a.idx_out = c->r.idx;
+  a.w_out = c->r.w;
   a.x = x;
   a.rows = c->b1_rows;
   a.tsc = c->tsc;
@@ -633,7 +627,7 @@ cudaError_t launch_experts_b1(const moe_ctx* c, const __nv_bfloat16* x, __nv_bfl
                       : launch_pdl(experts_b1_kernel<4096>, dim3(c->b1_grid), dim3(kB1Threads), c->b1_smem, s, a);
   if (e != cudaSuccess) return e;
   DnArgs d;
-  d.idx_in = c->r.idx;
+  d.logits = c->logits;
   d.h = c->h;
   d.x = x;
   d.y = y;

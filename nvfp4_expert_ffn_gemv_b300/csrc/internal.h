@@ -50,7 +50,6 @@ struct moe_ctx {
   float* router_t = nullptr;     // [E][d]
   uint8_t* b1_rows = nullptr;    // [n_all][f][1.125 d] gate/up records per hidden row
   float* logits = nullptr;       // [E]
-  unsigned* ticket = nullptr;    // CTA completion counters, zero between calls
 
   // prefill (see prefill.cu)
   int pf_enabled = 0;

@@ -83,7 +83,6 @@ size_t carve(moe_ctx* x, uint8_t* base) {
     x->router_t = cv.take<float>(base, d * E);
     x->b1_rows = cv.take<uint8_t>(base, n * f * b1_row_bytes((int)d));
     x->logits = cv.take<float>(base, E);
-    x->ticket = cv.take<unsigned>(base, 4);
   }
   x->max_positions = (int)P;
   if (x->mma_enabled) {
@@ -271,7 +270,6 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
   }
   if (e == cudaSuccess && x->b1_enabled) {
     e = repack_b1_layouts(x);
-    if (e == cudaSuccess) e = cudaMemset(x->ticket, 0, sizeof(unsigned) * 4);
     if (e == cudaSuccess) e = prepare_b1_kernels(x);
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
