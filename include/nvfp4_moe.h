@@ -168,6 +168,14 @@ MOE_API moe_status moe_quantize_nvfp4(const float* w, int n, int rows, int K, ui
 MOE_API moe_status moe_debug_prefill_h(moe_ctx* ctx, int T, uint8_t* h_codes, uint8_t* h_scales,
                                cudaStream_t stream);
 
+/* Copy the routing of the last forward call (moe_forward_decode with T >= 2,
+ * moe_forward_prefill, or moe_route) to the caller: idx [T][top_k] int32 and
+ * w [T][top_k] fp32, device pointers.  T must be that call's T.  Prefill from
+ * 256 tokens up computes its logits on the tensor cores, in another order of
+ * fp32 additions than moe_route, so on a near-tie the two may pick different
+ * experts; this call returns the ones prefill used.  For checking only. */
+MOE_API moe_status moe_debug_routing(moe_ctx* ctx, int T, int32_t* idx, float* w, cudaStream_t stream);
+
 /* Record `start` / `stop` (cudaEvent_t, may be NULL to disable) around the
  * expert kernels of every following forward call on its stream.  The records
  * are external event records, so inside a stream capture they become event

@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 #: every symbol the C header declares
 EXPORTS = ("moe_init", "moe_route", "moe_route_noalloc", "moe_forward_decode", "moe_forward_prefill", "moe_quantize_nvfp4",
-           "moe_debug_prefill_h", "moe_set_profile_events", "moe_get_device_status",
+           "moe_debug_prefill_h", "moe_debug_routing", "moe_set_profile_events", "moe_get_device_status",
            "moe_kernels_per_forward", "moe_destroy", "moe_status_string")
 
 
@@ -68,6 +68,7 @@ def _load():
         "moe_forward_prefill": (i, [vp, vp, i, vp, i, vp]),
         "moe_quantize_nvfp4": (i, [vp, i, i, i, vp, vp, vp, vp]),
         "moe_debug_prefill_h": (i, [vp, i, vp, vp, vp]),
+        "moe_debug_routing": (i, [vp, i, vp, vp, vp]),
         "moe_set_profile_events": (i, [vp, vp, vp]),
         "moe_get_device_status": (i, [vp]),
         "moe_kernels_per_forward": (i, [vp, i, i]),
@@ -164,6 +165,10 @@ def moe_quantize_nvfp4(w, n: int, rows: int, K: int, codes, scales, ts, stream=N
 def moe_debug_prefill_h(ctx, T: int, h_codes, h_scales, stream=None) -> None:
     _check("moe_debug_prefill_h", _lib.moe_debug_prefill_h(ctx, int(T), _ptr(h_codes), _ptr(h_scales),
                                                            _stream(stream)))
+
+
+def moe_debug_routing(ctx, T: int, idx, w, stream=None) -> None:
+    _check("moe_debug_routing", _lib.moe_debug_routing(ctx, int(T), _ptr(idx), _ptr(w), _stream(stream)))
 
 
 def moe_set_profile_events(ctx, start=None, stop=None) -> None:

@@ -43,6 +43,12 @@ struct moe_ctx {
   uint8_t* x16 = nullptr;        // [max_tokens][d] f16, prescaled, k-permuted
   float* xunshift = nullptr;     // [max_tokens]
 
+  // tensor-core router for long batches (see router_tc.cu)
+  int rt_enabled = 0;
+  __nv_bfloat16* rt_wsplit = nullptr;  // [3][Ep][d] bf16 splits of W_r^T
+  float* rt_part = nullptr;            // [kRTcChunks][max_tokens][E] partial logits
+  CUtensorMap rt_tmw;
+
   // batch-1 decode fast path (see decode_b1.cu / repack.cu)
   int b1_enabled = 0;
   int b1_grid = 0, b1_rmax = 0, b1_nbmax = 0;
@@ -80,6 +86,14 @@ cudaError_t launch_combine(const moe_ctx* c, const __nv_bfloat16* x, int T, __nv
 cudaError_t launch_quantize_nvfp4(const float* w, int n, int rows, int K, uint8_t* codes,
                                   uint8_t* scales, float* ts, cudaStream_t s);
 int router_chunks(int d, int T);
+cudaError_t launch_router_topk(const float* part, const float* bias, int has_bias, int T, int E, int K, int nkc,
+                               int32_t* idx, float* w, int* status, cudaStream_t s);
+constexpr int kRTcChunks = 4;   // K chunks of the tensor-core router
+constexpr int kRTcMinTokens = 256;
+int router_tc_padded_experts(const moe_config& c);
+bool router_tc_supported(const moe_config& c);
+cudaError_t router_tc_prepare(moe_ctx* c);
+cudaError_t launch_router_tc(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
 cudaError_t prepare_router_kernels();
 // Allocation-free router (split-K partials in a static device array, see router.cu).
 size_t router_static_capacity();

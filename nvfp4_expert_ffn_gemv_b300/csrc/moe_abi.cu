@@ -85,6 +85,10 @@ size_t carve(moe_ctx* x, uint8_t* base) {
     x->logits = cv.take<float>(base, E);
   }
   x->max_positions = (int)P;
+  if (x->rt_enabled) {
+    x->rt_wsplit = cv.take<__nv_bfloat16>(base, (size_t)3 * router_tc_padded_experts(c) * d);
+    x->rt_part = cv.take<float>(base, (size_t)kRTcChunks * T * E);
+  }
   if (x->mma_enabled) {
     x->x16 = cv.take<uint8_t>(base, T * d * 2);
     x->xunshift = cv.take<float>(base, T);
@@ -191,6 +195,7 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
   }
   x->pf_enabled = prefill_supported(c);
   x->mma_enabled = mma_decode_supported(c);
+  x->rt_enabled = x->pf_enabled && router_tc_supported(c) && c.max_tokens >= kRTcMinTokens;
   x->arena_bytes = carve(x, nullptr);
   if (cudaMalloc(&x->arena, x->arena_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -263,6 +268,7 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
   if (e == cudaSuccess) e = prepare_bucket_kernel();
   if (e == cudaSuccess) e = prepare_decode_kernels(x);
   if (e == cudaSuccess && x->mma_enabled) e = prepare_mma_decode(x);
+  if (e == cudaSuccess && x->rt_enabled) e = router_tc_prepare(x);
   if (e == cudaSuccess && x->pf_enabled) {
     e = prefill_prepare(x);
     if (e == cudaSuccess) e = cudaMemset(x->pf_hq, 0, prefill_max_rows(c) * (f / 2));
@@ -378,7 +384,11 @@ moe_status moe_forward_prefill(moe_ctx* x, const void* x_bf16, int T, void* y_bf
   if (T == 0) return MOE_OK;
   ensure_device(x->device);
   const auto* xb = static_cast<const __nv_bfloat16*>(x_bf16);
-  CK(launch_router(x, xb, T, s));
+  if (x->rt_enabled && T >= kRTcMinTokens) {
+    CK(launch_router_tc(x, xb, T, s));
+  } else {
+    CK(launch_router(x, xb, T, s));
+  }
   CK(launch_bucket(x, T, s));
   if (x->prof_start) CK(cudaEventRecordWithFlags(x->prof_start, s, cudaEventRecordExternal));
   CK(launch_prefill_experts(x, xb, T, s));
@@ -394,6 +404,16 @@ moe_status moe_debug_prefill_h(moe_ctx* x, int T, uint8_t* h_codes, uint8_t* h_s
   if (T != x->last_prefill_T) return MOE_ERR_INVALID_ARG;
   ensure_device(x->device);
   CK(launch_gather_prefill_h(x, T, h_codes, h_scales, s));
+  return MOE_OK;
+}
+
+moe_status moe_debug_routing(moe_ctx* x, int T, int32_t* idx, float* w, cudaStream_t s) {
+  if (!x || !idx || !w || T < 0 || T > x->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  ensure_device(x->device);
+  const size_t tk = (size_t)T * x->cfg.top_k;
+  CK(cudaMemcpyAsync(idx, x->r.idx, tk * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+  CK(cudaMemcpyAsync(w, x->r.w, tk * sizeof(float), cudaMemcpyDeviceToDevice, s));
   return MOE_OK;
 }
 

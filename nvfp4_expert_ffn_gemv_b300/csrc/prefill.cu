@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int u = blockIdx.x; u < U; u += gridDim.x, ++i) {
       const UnitInfo ui = decode_unit(tab, u, ntiles, na);
       const int buf = i & 1;
-      const bool ok = bounded_wait(&dfull_bar[buf], (i >> 1) & 1);
+      const bool ok = __all_sync(0xffffffffu, bounded_wait(&dfull_bar[buf], (i >> 1) & 1));   // warp-uniform
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * kBN;
       const float* ts = g.tsc + ui.e * 3;

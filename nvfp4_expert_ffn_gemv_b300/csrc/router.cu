@@ -263,27 +263,29 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
   warp_select(v, E, K, t, idx, wout, status);
 }
 
-// Few K chunks (nkc <= 2): one warp per token, the same sums in the same order.
+// Few K chunks (nkc <= 4): one warp per token, the same sums in the same order.
 __global__ void __launch_bounds__(256) router_topk_warp_kernel(
     const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
     int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  float p0[8], p1[8];
+  float p[4][8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int ee = lane + 32 * i;
-    p0[i] = ee < E ? __ldg(part + (size_t)t * E + ee) : 0.f;
-    p1[i] = (ee < E && nkc > 1) ? __ldg(part + ((size_t)T + t) * E + ee) : 0.f;
-  }
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int ee = lane + 32 * i;
+      p[q][i] = (ee < E && q < nkc) ? __ldg(part + ((size_t)q * T + t) * E + ee) : 0.f;
+    }
   float v[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int ee = lane + 32 * i;
     float s = 0.f;
-    s += p0[i];
-    if (nkc > 1) s += p1[i];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (q < nkc) s += p[q][i];
     if (ee < E && has_bias) s += bias[ee];
     v[i] = s;
   }
@@ -291,6 +293,19 @@ __global__ void __launch_bounds__(256) router_topk_warp_kernel(
 }
 
 int router_tile(int T) { return T >= 256 ? 32 : 8; }
+
+}  // namespace
+
+cudaError_t launch_router_topk(const float* part, const float* bias, int has_bias, int T, int E, int K, int nkc,
+                               int32_t* idx, float* w, int* status, cudaStream_t s) {
+  if (nkc <= 4)
+    router_topk_warp_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status);
+  else
+    router_topk_kernel<<<T, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status);
+  return cudaGetLastError();
+}
+
+namespace {
 
 cudaError_t launch_router_kernels(const __nv_bfloat16* x, int T, const float* wr, const float* bias,
                                   int has_bias, int d, int E, int K, float* part, int32_t* idx, float* w,
@@ -307,11 +322,7 @@ cudaError_t launch_router_kernels(const __nv_bfloat16* x, int T, const float* wr
     router_partial_kernel<8><<<g1, 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  if (nkc <= 2)
-    router_topk_warp_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status);
-  else
-    router_topk_kernel<<<T, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status);
-  return cudaGetLastError();
+  return launch_router_topk(part, bias, has_bias, T, E, K, nkc, idx, w, status, s);
 }
 
 // Scratch of the allocation-free router entry point: the split-K partial

@@ -115,7 +115,8 @@ def _check_prefill(lib, layer, xb, x, T, sample=None):
     hs = torch.empty((slots, f // 16), dtype=torch.uint8, device="cuda")
     lib.moe_debug_prefill_h(layer.ctx, T, hc, hs)
     idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
-    lib.moe_route(layer.ctx, xb, T, idx)
+    wsel = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    lib.moe_debug_routing(layer.ctx, T, idx, wsel)     # the experts this prefill used
     torch.cuda.synchronize()
     assert lib.moe_get_device_status(layer.ctx) == 0
     idx = idx.cpu().numpy()
