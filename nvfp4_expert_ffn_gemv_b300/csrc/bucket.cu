@@ -148,6 +148,38 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T
       *r.n_active = na;
       if (total != T * k) latch_status(status, MOE_ERR_DEVICE_CHECK);
     }
+    // padded 128-row blocks of the active experts (prefill's GEMM tiles) and
+    // the active expert of every block, in the same compaction order
+    int pl = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pl += (local[i] + 127) >> 7;
+    int pincl = pl;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, pincl, o);
+      if (lane >= o) pincl += v;
+    }
+    int blk = pincl - pl, a2 = aincl - lact;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (local[i] > 0) {
+        const int nb = (local[i] + 127) >> 7;
+        r.act_ppos[a2] = blk * 128;
+        for (int b = 0; b < nb; ++b) r.blk_a[blk + b] = a2;
+        blk += nb;
+        ++a2;
+      }
+    }
+    const int rblocks = __shfl_sync(0xffffffffu, pincl, 31);
+    const int nact2 = __shfl_sync(0xffffffffu, aincl, 31);
+    int sblk = rblocks;
+    const int snb = (T + 127) >> 7;
+    for (int s2 = 0; s2 < (T > 0 ? S : 0); ++s2) {
+      if (lane == 0) r.act_ppos[nact2 + s2] = sblk * 128;
+      for (int b = lane; b < snb; b += 32) r.blk_a[sblk + b] = nact2 + s2;
+      sblk += snb;
+    }
+    if (lane == 0) r.act_ppos[nact2 + (T > 0 ? S : 0)] = sblk * 128;
   }
   __syncthreads();
 
@@ -163,7 +195,6 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T
       if (e < 0 || e >= E) e = 0;
       p = off[e] + r.chunk_cnt[(size_t)(t >> 5) * E + e] + r.rank[s];
     }
-    r.perm[p] = s;
     r.slot_pos[s] = p;
     r.pos_tok[p] = t;
   }

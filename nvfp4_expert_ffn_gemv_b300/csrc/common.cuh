@@ -122,7 +122,6 @@ struct Routing {
   float* w;            // [T][k]
   int32_t* counts;     // [E]
   int32_t* offsets;    // [E+1]
-  int32_t* perm;       // [T*k] position -> slot t*k+j
   int32_t* slot_pos;   // [T*k] slot -> position
   int32_t* pos_tok;    // [T*k + S*T] position -> token
   int32_t* act_e;      // [E+S] active experts (count > 0), shared last
@@ -130,7 +129,7 @@ struct Routing {
   int32_t* act_n;      // [E+S] tokens of each active expert
   int32_t* n_active;   // [1]
   int32_t* act_ppos;   // [E+S+1] prefill: padded first row (multiple of 128), total last
-  int32_t* act_ntb;    // [E+S+1] prefill: first 256-token N tile, total last
+  int32_t* blk_a;      // [padded rows / 128] prefill: active expert of each 128-row block
   int32_t* chunk_cnt;  // [ceil(T/32)][E] scratch
   int32_t* rank;       // [T*k] scratch
 };

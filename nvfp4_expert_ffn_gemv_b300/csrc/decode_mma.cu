@@ -42,7 +42,7 @@ namespace nvmoe {
 namespace {
 
 constexpr int kThreads = 256;   // 8 warps x 16 weight rows = 128 rows per tile
-constexpr int kTok = 16;        // tokens (positions) per tile: two MMA column groups of 8
+constexpr int kTok = 8;         // tokens (positions) per tile: one MMA column group
 constexpr int kChunk = 128;     // k per chunk
 
 // ---------------------------------------------------------------------------
@@ -226,10 +226,10 @@ struct GuSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) gateup_mma_kernel(MmaArgs g) {
+__global__ void __launch_bounds__(kThreads, 4) gateup_mma_kernel(MmaArgs g) {
   using L = GuSmem<D>;
   constexpr int NCH = D / kChunk;        // 128-wide k chunks
-  constexpr int B = NCH < 4 ? NCH : 4;   // chunks per register batch
+  constexpr int B = 2;                   // chunks per register batch
   constexpr int NB = NCH / B;
   extern __shared__ __align__(16) uint8_t sm[];
   float* sG = reinterpret_cast<float*>(sm + L::kG);
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_mma_kernel(MmaArgs g) {
     float* dst = warp < 4 ? sG : sU;
     const int j0 = (warp & 3) * 16 + gq;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < kTok / 8; ++q) {
       const int col = q * 8 + 2 * c;
       dst[j0 * (kTok + 1) + col] = acc[q][0] * ts * sUn[col];
       dst[j0 * (kTok + 1) + col + 1] = acc[q][1] * ts * sUn[col + 1];
@@ -368,10 +368,10 @@ struct DnSmem {
 };
 
 template <int F>
-__global__ void __launch_bounds__(kThreads, 2) down_mma_kernel(MmaArgs g) {
+__global__ void __launch_bounds__(kThreads, 4) down_mma_kernel(MmaArgs g) {
   using L = DnSmem<F>;
   constexpr int NCH = F / kChunk;
-  constexpr int B = NCH < 4 ? NCH : 4;
+  constexpr int B = NCH < 2 ? NCH : 2;
   constexpr int NB = NCH / B;
   extern __shared__ __align__(16) uint8_t sm[];
   float* sY = reinterpret_cast<float*>(sm + L::kY);
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_mma_kernel(MmaArgs g) {
     const float ts = g.tsc[e * 3 + 2];
     const int r0 = warp * 16 + gq;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < kTok / 8; ++q) {
       const int col = q * 8 + 2 * c;
       sY[col * 132 + r0] = acc[q][0] * ts * sUn[col];
       sY[(col + 1) * 132 + r0] = acc[q][1] * ts * sUn[col + 1];
@@ -581,7 +581,7 @@ cudaError_t launch_mma_decode(const moe_ctx* c, const __nv_bfloat16* x, int T, c
   xprep_kernel<<<(T + 7) / 8, 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int grid = 2 * c->sm_count;
+  const int grid = 4 * c->sm_count;
   const size_t gs = gu_smem(c), ds = dn_smem(c);
   switch (a.d) {
     case 256: gateup_mma_kernel<256><<<grid, kThreads, gs, s>>>(a); break;

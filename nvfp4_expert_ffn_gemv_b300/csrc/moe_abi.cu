@@ -65,7 +65,6 @@ size_t carve(moe_ctx* x, uint8_t* base) {
   x->r.w = cv.take<float>(base, T * k);
   x->r.counts = cv.take<int32_t>(base, E);
   x->r.offsets = cv.take<int32_t>(base, E + 1);
-  x->r.perm = cv.take<int32_t>(base, T * k);
   x->r.slot_pos = cv.take<int32_t>(base, T * k);
   x->r.pos_tok = cv.take<int32_t>(base, P);
   x->r.act_e = cv.take<int32_t>(base, E + S);
@@ -73,7 +72,7 @@ size_t carve(moe_ctx* x, uint8_t* base) {
   x->r.act_n = cv.take<int32_t>(base, E + S);
   x->r.n_active = cv.take<int32_t>(base, 1);
   x->r.act_ppos = cv.take<int32_t>(base, E + S + 1);
-  x->r.act_ntb = cv.take<int32_t>(base, E + S + 1);
+  x->r.blk_a = cv.take<int32_t>(base, (T * (k + S) + 127) / 128 + E + S);
   x->r.chunk_cnt = cv.take<int32_t>(base, ((T + 31) / 32) * E);
   x->r.rank = cv.take<int32_t>(base, T * k);
   x->h = cv.take<float>(base, P * f);
@@ -447,7 +446,7 @@ moe_status moe_get_device_status(moe_ctx* x) {
 int moe_kernels_per_forward(moe_ctx* x, int T, int prefill) {
   if (!x || T <= 0) return 0;
   if (!prefill && T == 1 && x->b1_enabled) return 3;
-  if (prefill) return 9;   // router x2, bucket, plan, quantise x, gather x, GEMM x2, combine
+  if (prefill) return 8;   // router x2, bucket, quantise x, gather x, GEMM x2, combine
   if (x->mma_enabled) return 7;   // router x2, bucket, x prescale, gate/up, down, combine
   return 6;
 }

@@ -9,7 +9,8 @@
 // expert), so it runs on the tensor cores with both operands in NVFP4:
 //
 //   1. plan:   padded position blocks per active expert (multiples of 128
-//              tokens, so every 128-row block belongs to one expert);
+//              tokens, so every 128-row block belongs to one expert), made by
+//              the bucketing kernel;
 //   2. x -> NVFP4 (16-element E4M3 block scales, tensor scale 1) gathered into
 //              the padded blocks, scales written straight into the
 //              scale-factor atoms the MMA reads;
@@ -63,29 +64,6 @@ constexpr int kOffB = kOffA + kStages * kA;
 constexpr int kOffSFA = kOffB + kStages * kB;
 constexpr int kOffSFB = kOffSFA + kStages * kSF;
 constexpr int kSmemGemm = kOffSFB + kStages * kSF + 1024;  // + alignment slack
-
-// ---------------------------------------------------------------------------
-// plan: padded positions and N-tile prefix per active expert (one warp)
-// ---------------------------------------------------------------------------
-__global__ void prefill_plan_kernel(Routing r) {
-  const int lane = threadIdx.x;
-  const int na = *r.n_active;
-  int pp = 0;
-  for (int base = 0; base < na; base += 32) {
-    const int a = base + lane;
-    const int n = a < na ? r.act_n[a] : 0;
-    const int vp = (n + 127) / 128 * 128;
-    int ip = vp;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int up = __shfl_up_sync(0xffffffffu, ip, o);
-      if (lane >= o) ip += up;
-    }
-    if (a < na) r.act_ppos[a] = pp + ip - vp;
-    pp += __shfl_sync(0xffffffffu, ip, 31);
-  }
-  if (lane == 0) r.act_ppos[na] = pp;
-}
 
 // largest a < na with tab[a] <= v (tab non-decreasing, tab[0] = 0)
 __device__ __forceinline__ int find_seg(const int32_t* tab, int na, int v) {
@@ -166,7 +144,7 @@ __global__ void __launch_bounds__(256) gather_x_kernel(Routing r, const uint8_t*
   const int na = *r.n_active;
   const int total = r.act_ppos[na];
   if (p >= total || p >= max_rows) return;
-  const int a = find_seg(r.act_ppos, na, p);
+  const int a = r.blk_a[p >> 7];
   const int i = p - r.act_ppos[a];
   const bool real = i < r.act_n[a];
   const int t = real ? r.pos_tok[r.act_pos[a] + i] : 0;
@@ -524,9 +502,7 @@ cudaError_t prefill_prepare(moe_ctx* c) {
 cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s) {
   const int d = c->cfg.d_model, f = c->cfg.d_ff;
   const int rows = (int)prefill_max_rows(c->cfg);
-  prefill_plan_kernel<<<1, 32, 0, s>>>(c->r);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   quant_tokens_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, d, c->pf_xq_tok, c->pf_xsf_tok);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gather_x_kernel<<<(rows + 7) / 8, 256, 0, s>>>(c->r, c->pf_xq_tok, c->pf_xsf_tok, d, c->pf_xq, c->pf_xsf, rows);
