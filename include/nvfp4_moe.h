@@ -177,7 +177,8 @@ MOE_API moe_status moe_debug_prefill_h(moe_ctx* ctx, int T, uint8_t* h_codes, ui
 MOE_API moe_status moe_debug_routing(moe_ctx* ctx, int T, int32_t* idx, float* w, cudaStream_t stream);
 
 /* Record `start` / `stop` (cudaEvent_t, may be NULL to disable) around the
- * expert kernels of every following forward call on its stream.  The records
+ * expert kernels of every following forward call on its stream (for a
+ * batch-1 decode: around its whole router -> experts -> down chain).  The records
  * are external event records, so inside a stream capture they become event
  * record nodes of the graph and can be timed after a replay. */
 MOE_API moe_status moe_set_profile_events(moe_ctx* ctx, cudaEvent_t start, cudaEvent_t stop);

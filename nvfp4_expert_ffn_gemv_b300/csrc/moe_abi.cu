@@ -353,8 +353,9 @@ moe_status moe_forward_decode(moe_ctx* x, const void* x_bf16, int T, void* y_bf1
   ensure_device(x->device);
   const auto* xb = static_cast<const __nv_bfloat16*>(x_bf16);
   if (T == 1 && x->b1_enabled) {
-    CK(launch_router_b1(x, xb, s));
+    // the three kernels of a token form one PDL chain: profile it as a whole
     if (x->prof_start) CK(cudaEventRecordWithFlags(x->prof_start, s, cudaEventRecordExternal));
+    CK(launch_router_b1(x, xb, s));
     CK(launch_experts_b1(x, xb, static_cast<__nv_bfloat16*>(y_bf16), residual, s));
     if (x->prof_stop) CK(cudaEventRecordWithFlags(x->prof_stop, s, cudaEventRecordExternal));
     return MOE_OK;
