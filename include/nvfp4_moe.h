@@ -68,10 +68,10 @@ typedef enum {
 typedef enum { MOE_W_NVFP4 = 0, MOE_W_BF16 = 1 } moe_weight_format;
 
 typedef struct {
-  int d_model;        /* hidden size, multiple of 256, <= 8192                  */
+  int d_model;        /* hidden size: 256, 512, 1024, 2048 or 4096               */
   int n_experts;      /* routed experts, 1..256                                  */
   int top_k;          /* experts chosen per token, 1..min(8, n_experts)          */
-  int d_ff;           /* expert width, one of 64, 128, 256, 512, 1024            */
+  int d_ff;           /* expert width: 128, 256, 512 or 1024                     */
   int n_shared;       /* always-on shared experts, 0..2                          */
   int d_ff_shared;    /* width of the shared experts; must equal d_ff            */
   int max_tokens;     /* largest T any forward call will pass, 1..65536          */
