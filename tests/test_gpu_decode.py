@@ -94,6 +94,19 @@ def _check_layer(lib, layer, xb, x, T, per_token=False, residual=0, prefix=""):
     assert np.array_equal(counts, ref.counts)
     assert np.allclose(w, ref.w, rtol=2e-6, atol=1e-7)
     y = _run_decode(lib, layer, xb, T, residual=residual, per_token=per_token)
+    if not per_token:
+        # the forward call may route with another kernel than moe_route (other fp32
+        # summation order): it must agree except on the oracle's near-ties, and the
+        # output is checked against the experts it actually used
+        fidx = torch.empty((T, layer.shape.top_k), dtype=torch.int32, device="cuda")
+        fw = torch.empty((T, layer.shape.top_k), dtype=torch.float32, device="cuda")
+        lib.moe_debug_routing(layer.ctx, T, fidx, fw)
+        fidx = fidx.cpu().numpy()
+        if not np.array_equal(fidx, idx):
+            harness.check_routing(fidx, omoe.moe_layer(lw, x, layer.shape.top_k, layer.shape.n_shared))
+            lw = layer.oracle_weights(np.concatenate([fidx.ravel(), idx.ravel(),
+                                                      np.arange(layer.shape.n_experts, layer.shape.n_all)]))
+            ref = omoe.moe_layer(lw, x, layer.shape.top_k, layer.shape.n_shared, force_idx=fidx)
     want = ref.y_bf16 if not residual else omoe.residual(x, ref.y)
     return harness.assert_close(y, want, f"{prefix} T={T}")
 
