@@ -103,16 +103,31 @@ __device__ __forceinline__ int prescale_shift(uint32_t amax_bits) {
 // k = 32c + 4kk + 0..3
 __device__ __forceinline__ int perm_off(int c, int kk) { return (kk * 4 + c) * 8; }
 
-// A fragments of one MMA step from a quad's code bytes: rows g and g+8 each
-// contribute the 2 code bytes 2kk, 2kk+1 of their 16-byte slice, times the
-// block scale (f16x2 broadcast).
-__device__ __forceinline__ void a_frag(uint32_t (&a)[4], uint32_t wg, uint32_t wg8, int kk, uint32_t sg,
-                                       uint32_t sg8) {
-  const int sh = (kk & 1) * 16;
-  a[0] = hmul2(cvt_e2m1x2_f16x2((wg >> sh) & 0xFF), sg);
-  a[2] = hmul2(cvt_e2m1x2_f16x2((wg >> (sh + 8)) & 0xFF), sg);
-  a[1] = hmul2(cvt_e2m1x2_f16x2((wg8 >> sh) & 0xFF), sg8);
-  a[3] = hmul2(cvt_e2m1x2_f16x2((wg8 >> (sh + 8)) & 0xFF), sg8);
+// Eight E2M1 codes (one word, element 2j in the low nibble of byte j) -> four
+// exact f16x2, one mov splitting the word into bytes and four hardware cvts.
+__device__ __forceinline__ void cvt_e2m1x8(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
+}
+
+// A fragments of the two MMA steps 2w and 2w+1 from word w of the quad's code
+// slice of rows g (wg) and g+8 (wg8): bytes 0, 1 feed step 2w, bytes 2, 3 step
+// 2w+1; every f16x2 is multiplied by its row's block scale (exact).
+__device__ __forceinline__ void a_frag_pair(uint32_t (&a0)[4], uint32_t (&a1)[4], uint32_t wg, uint32_t wg8,
+                                            uint32_t sg, uint32_t sg8) {
+  uint32_t g[4], h[4];
+  cvt_e2m1x8(wg, g);
+  cvt_e2m1x8(wg8, h);
+  a0[0] = hmul2(g[0], sg);
+  a0[2] = hmul2(g[1], sg);
+  a0[1] = hmul2(h[0], sg8);
+  a0[3] = hmul2(h[1], sg8);
+  a1[0] = hmul2(g[2], sg);
+  a1[2] = hmul2(g[3], sg);
+  a1[1] = hmul2(h[2], sg8);
+  a1[3] = hmul2(h[3], sg8);
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
@@ -307,17 +322,21 @@ __global__ void __launch_bounds__(kThreads, 4) gateup_mma_kernel(MmaArgs g) {
         const int ch = b * B + i;
         const uint32_t s2 = cvt_e4m3x2_f16x2(ws[i]), s28 = cvt_e4m3x2_f16x2(ws8[i]);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t sg = kk < 4 ? bcast_lo(s2) : bcast_hi(s2);
-          const uint32_t sg8 = kk < 4 ? bcast_lo(s28) : bcast_hi(s28);
-          uint32_t af[4];
-          a_frag(af, word_of(wc[i], kk >> 1), word_of(wc8[i], kk >> 1), kk, sg, sg8);
-          const int off = ch * kChunk * 2 + perm_off(c, kk);
-          const uint2 b0 = lds64(xrow0 + off);
-          mma_f16(acc[0], af, b0.x, b0.y);
-          if (two) {
-            const uint2 b1 = lds64(xrow1 + off);
-            mma_f16(acc[1], af, b1.x, b1.y);
+        for (int wd = 0; wd < 4; ++wd) {
+          const uint32_t sg = wd < 2 ? bcast_lo(s2) : bcast_hi(s2);
+          const uint32_t sg8 = wd < 2 ? bcast_lo(s28) : bcast_hi(s28);
+          uint32_t afp[2][4];
+          a_frag_pair(afp[0], afp[1], word_of(wc[i], wd), word_of(wc8[i], wd), sg, sg8);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int kk = 2 * wd + h2;
+            const int off = ch * kChunk * 2 + perm_off(c, kk);
+            const uint2 b0 = lds64(xrow0 + off);
+            mma_f16(acc[0], afp[h2], b0.x, b0.y);
+            if (two) {
+              const uint2 b1 = lds64(xrow1 + off);
+              mma_f16(acc[1], afp[h2], b1.x, b1.y);
+            }
           }
         }
       }
@@ -460,19 +479,23 @@ __global__ void __launch_bounds__(kThreads, 4) down_mma_kernel(MmaArgs g) {
         const int ch = b * B + i;
         const uint32_t s2 = cvt_e4m3x2_f16x2(ws[i]), s28 = cvt_e4m3x2_f16x2(ws8[i]);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t sg = kk < 4 ? bcast_lo(s2) : bcast_hi(s2);
-          const uint32_t sg8 = kk < 4 ? bcast_lo(s28) : bcast_hi(s28);
-          uint32_t af[4];
-          a_frag(af, word_of(wc[i], kk >> 1), word_of(wc8[i], kk >> 1), kk, sg, sg8);
-          const int off = ch * kChunk * 2 + perm_off(c, kk);
-          const uint2 bh = lds64(hi0 + off), bl = lds64(lo0 + off);
-          mma_f16(acc[0], af, bh.x, bh.y);
-          mma_f16(acc[0], af, bl.x, bl.y);
-          if (two) {
-            const uint2 bh1 = lds64(hi0 + 8 * L::kHRow + off), bl1 = lds64(lo0 + 8 * L::kHRow + off);
-            mma_f16(acc[1], af, bh1.x, bh1.y);
-            mma_f16(acc[1], af, bl1.x, bl1.y);
+        for (int wd = 0; wd < 4; ++wd) {
+          const uint32_t sg = wd < 2 ? bcast_lo(s2) : bcast_hi(s2);
+          const uint32_t sg8 = wd < 2 ? bcast_lo(s28) : bcast_hi(s28);
+          uint32_t afp[2][4];
+          a_frag_pair(afp[0], afp[1], word_of(wc[i], wd), word_of(wc8[i], wd), sg, sg8);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int kk = 2 * wd + h2;
+            const int off = ch * kChunk * 2 + perm_off(c, kk);
+            const uint2 bh = lds64(hi0 + off), bl = lds64(lo0 + off);
+            mma_f16(acc[0], afp[h2], bh.x, bh.y);
+            mma_f16(acc[0], afp[h2], bl.x, bl.y);
+            if (two) {
+              const uint2 bh1 = lds64(hi0 + 8 * L::kHRow + off), bl1 = lds64(lo0 + 8 * L::kHRow + off);
+              mma_f16(acc[1], afp[h2], bh1.x, bh1.y);
+              mma_f16(acc[1], afp[h2], bl1.x, bl1.y);
+            }
           }
         }
       }
