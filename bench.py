@@ -152,6 +152,18 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(value: float, device: str = "cuda") -> float:
+    """The largest of every rank's value (the whole job ends with its slowest rank);
+    the value itself when the job has one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -282,10 +294,7 @@ def run_ours(args):
         gp.replay()
     torch.cuda.synchronize()
     kern_ms = sorted(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms)
 
     # end to end: pinned host tokens in, host result out, every step
     xh = x[:chunk].cpu().pin_memory()
@@ -309,10 +318,7 @@ def run_ours(args):
         ge.replay()
     torch.cuda.synchronize()
     e2e_ms = timed(ge, replays)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms)
 
     # algorithmic bytes of a batched-decode step: every distinct chosen expert once, plus the shared one
     distinct_mean, distinct_bytes = 0.0, 0
