@@ -58,6 +58,8 @@ WORKLOADS = {
                   metric="MoE decode tok/s (batch-1, 47-layer Flint MoE stack, attention omitted)"),
     "prefill": dict(T=4096, layers=16, steps=40, chunk=4,
                     metric="MoE prefill tok/s (4096 tokens, one Flint-shaped NVFP4 MoE layer)"),
+    "prefill_32k": dict(T=32768, layers=4, steps=8, chunk=2,
+                        metric="MoE prefill tok/s (32768 tokens, one Flint-shaped NVFP4 MoE layer)"),
 }
 
 
@@ -216,7 +218,7 @@ def run_ours(args):
     replays = (K + chunk - 1) // chunk
     K = replays * chunk
     stack = args.workload == "stack"
-    prefill = args.workload == "prefill"
+    prefill = args.workload.startswith("prefill")
     bias = synth.zipf_bias(s, seed=4242) if args.workload == "decode_b64" else None
     ctxs = build_layers(lib, torch, synth, n_layers, max_tokens=T, bias=bias, seed0=100 * rank)
     stream = torch.cuda.Stream()
@@ -321,15 +323,25 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e2e_ms)
 
     # algorithmic bytes of a batched-decode step: every distinct chosen expert once, plus the shared one
-    distinct_mean, distinct_bytes = 0.0, 0
-    if args.workload == "decode_b64":
+    # expert load of the timed inputs (routing only, outside the timed region): distinct experts
+    # per step (the algorithmic bytes of a batched-decode step) and the max/mean tokens per expert
+    distinct_mean, distinct_bytes, load = 0.0, 0, None
+    if args.workload == "decode_b64" or prefill:
         idx = torch.empty((T, s.top_k), dtype=torch.int32, device="cuda")
-        counts = []
-        for i in range(chunk):
-            lib.moe_route(ctxs[i % n_layers], x[i], T, idx)
-            counts.append(int(torch.unique(idx).numel()))
-        distinct_mean = sum(counts) / len(counts)
+        cnt = torch.empty((s.n_experts,), dtype=torch.int32, device="cuda")
+        distinct, ratios, maxes = [], [], []
+        for i in range(min(chunk, 8)):
+            lib.moe_route(ctxs[i % n_layers], x[i], T, idx, None, cnt)
+            c = cnt.float()
+            used = c[c > 0]
+            distinct.append(int(used.numel()))
+            ratios.append(float(c.max() / c.mean()))
+            maxes.append(int(c.max()))
+        distinct_mean = sum(distinct) / len(distinct)
         distinct_bytes = (distinct_mean + s.n_shared) * EXPERT_BYTES
+        load = {"distinct_experts": round(distinct_mean, 2), "max_tokens_per_expert": max(maxes),
+                "mean_tokens_per_expert": round(T * s.top_k / s.n_experts, 2),
+                "max_over_mean": round(sum(ratios) / len(ratios), 3)}
     per_fwd = lib.moe_kernels_per_forward(ctxs[0], T, int(prefill))
     launches = K * per_fwd * (n_layers if stack else 1)
     for c in ctxs:
@@ -351,8 +363,8 @@ def run_ours(args):
                    "d_model": D_MODEL, "n_experts": N_EXP, "top_k": TOP_K,
                    "n_shared": N_SHARED, "d_ff": D_FF, "tokens_per_step": T, "layers": n_layers,
                    "l2": ("47 distinct layers, ~21 GB of weights" if stack else
-                          f"{n_layers} rotating layer copies (>= 7 GB, far above the 126 MB L2): "
-                          "no weight is re-read from L2 between steps"),
+                          f"{n_layers} rotating layer copies ({n_layers * 0.455:.1f} GB of NVFP4 experts, far above "
+                          "the 126 MB L2): no weight is re-read from L2 between steps"),
                    "parallelism": "independent replicas" if world > 1 else "single GPU"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -404,6 +416,8 @@ def run_ours(args):
                             "algorithmic_bytes_per_launch": int(alg), "traffic": traffic, "launch_us": kus,
                             "distinct_experts_per_step": round(distinct_mean, 2)}
         line["expert_weight_gbs"] = round(alg * K / (ms / 1e3) / 1e9, 1)
+    if load is not None:
+        line["expert_load"] = load
     line["e2e"] = {"value": round(tok / (e2e_ms / 1e3), 1), "unit": "tok/s",
                    "h2d_bytes_per_step": T * D_MODEL * 2, "d2h_bytes_per_step": T * D_MODEL * 2}
     if not args.no_cpu_baseline:
@@ -437,7 +451,7 @@ def cpu_baseline(workload: str, budget_s: float = 10.0):
     from oracle import moe as omoe
 
     s = synth.FLINT
-    T = {"decode_b1": 1, "stack": 1, "decode_b64": 8, "prefill": 8}[workload]
+    T = {"decode_b1": 1, "stack": 1, "decode_b64": 8, "prefill": 8, "prefill_32k": 8}[workload]
     n_steps = 4 if T == 1 else 1
     router = synth.router_weight(s, synth.router_seed(0)).numpy()
     bias = synth.zipf_bias(s, seed=4242).numpy() if workload == "decode_b64" else None
@@ -473,7 +487,7 @@ def cpu_baseline(workload: str, budget_s: float = 10.0):
         done = 0
         while True:   # the sample's steps, repeated until about budget_s of CPU work
             i = done % n_steps
-            omoe.moe_layer(layers[i], x[i], s.top_k, s.n_shared, prefill=(workload == "prefill"))
+            omoe.moe_layer(layers[i], x[i], s.top_k, s.n_shared, prefill=workload.startswith("prefill"))
             done += 1
             if time.perf_counter() - t0 > budget_s:
                 break
@@ -483,7 +497,8 @@ def cpu_baseline(workload: str, budget_s: float = 10.0):
     what = {"decode_b1": "single-token decode steps through one layer",
             "stack": "single-token decode steps through one layer, divided by 47 layers",
             "decode_b64": "Zipf-skewed decode batch through one layer",
-            "prefill": "prefill-mode batch through one layer"}[workload]
+            "prefill": "prefill-mode batch through one layer",
+            "prefill_32k": "prefill-mode batch through one layer"}[workload]
     return {"value": round(value, 4), "unit": "tok/s", "cores": 1, "kind": "oracle",
             "sample": f"{done} x {T} token(s) ({n_steps} distinct step(s) repeated): {what} (numpy fp64 oracle, "
                       f"chosen experts dequantised each step), {dt:.2f} s timed"}

@@ -87,10 +87,16 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T
         run += v;
       }
     } else {
-      for (int c = 0; c < nchunks; ++c) {
-        const int v = r.chunk_cnt[(size_t)c * E + e];
-        r.chunk_cnt[(size_t)c * E + e] = run;
-        run += v;
+      // 32 loads in flight per batch (the stores of a batch follow all its loads)
+      for (int c0 = 0; c0 < nchunks; c0 += 32) {
+        int v[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = c0 + q < nchunks ? __ldcg(r.chunk_cnt + (size_t)(c0 + q) * E + e) : 0;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          if (c0 + q < nchunks) r.chunk_cnt[(size_t)(c0 + q) * E + e] = run;
+          run += v[q];
+        }
       }
     }
     cnt[e] = run;
