@@ -130,6 +130,15 @@ __device__ __forceinline__ void a_frag_pair(uint32_t (&a0)[4], uint32_t (&a1)[4]
   a1[3] = hmul2(h[3], sg8);
 }
 
+// Weight bytes are read once per call: a read-only load that does not allocate
+// in L1 (the L1 / shared-memory pipe is busy with the activation fragments).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
@@ -277,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 4) gateup_mma_kernel(MmaArgs g) {
     uint32_t ws[B], ws8[B];
 #pragma unroll
     for (int i = 0; i < B; ++i) {
-      wc[i] = __ldg(reinterpret_cast<const uint4*>(cg + i * 64));
-      wc8[i] = __ldg(reinterpret_cast<const uint4*>(cg8 + i * 64));
+      wc[i] = ld_stream16(cg + i * 64);
+      wc8[i] = ld_stream16(cg8 + i * 64);
       ws[i] = __ldg(reinterpret_cast<const uint16_t*>(sgp + i * 8));
       ws8[i] = __ldg(reinterpret_cast<const uint16_t*>(sg8p + i * 8));
     }
@@ -311,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 4) gateup_mma_kernel(MmaArgs g) {
 #pragma unroll
         for (int i = 0; i < B; ++i) {
           const int ch = (b + 1) * B + i;
-          nc[i] = __ldg(reinterpret_cast<const uint4*>(cg + ch * 64));
-          nc8[i] = __ldg(reinterpret_cast<const uint4*>(cg8 + ch * 64));
+          nc[i] = ld_stream16(cg + ch * 64);
+          nc8[i] = ld_stream16(cg8 + ch * 64);
           ns[i] = __ldg(reinterpret_cast<const uint16_t*>(sgp + ch * 8));
           ns8[i] = __ldg(reinterpret_cast<const uint16_t*>(sg8p + ch * 8));
         }
@@ -419,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 4) down_mma_kernel(MmaArgs g) {
     uint32_t ws[B], ws8[B];
 #pragma unroll
     for (int i = 0; i < B; ++i) {
-      wc[i] = __ldg(reinterpret_cast<const uint4*>(cg + i * 64));
-      wc8[i] = __ldg(reinterpret_cast<const uint4*>(cg8 + i * 64));
+      wc[i] = ld_stream16(cg + i * 64);
+      wc8[i] = ld_stream16(cg8 + i * 64);
       ws[i] = __ldg(reinterpret_cast<const uint16_t*>(sgp + i * 8));
       ws8[i] = __ldg(reinterpret_cast<const uint16_t*>(sg8p + i * 8));
     }
@@ -468,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 4) down_mma_kernel(MmaArgs g) {
 #pragma unroll
         for (int i = 0; i < B; ++i) {
           const int ch = (b + 1) * B + i;
-          nc[i] = __ldg(reinterpret_cast<const uint4*>(cg + ch * 64));
-          nc8[i] = __ldg(reinterpret_cast<const uint4*>(cg8 + ch * 64));
+          nc[i] = ld_stream16(cg + ch * 64);
+          nc8[i] = ld_stream16(cg8 + ch * 64);
           ns[i] = __ldg(reinterpret_cast<const uint16_t*>(sgp + ch * 8));
           ns8[i] = __ldg(reinterpret_cast<const uint16_t*>(sg8p + ch * 8));
         }
