@@ -292,6 +292,10 @@ __global__ void __launch_bounds__(kB1Threads, 1) experts_b1_kernel(B1Args a) {
   constexpr int CPL = D / 1024;  // 16-byte code chunks per lane per row
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* sm_gu = smem;                                                 // [rmax][gate/up record]
+  // x in fp32, float4 f of 32-column chunk c = l + 32q stored at float4 slot
+  // (8q + f) * 32 + l: the 32 lanes of a warp, each reading float4 f of its
+  // own chunk, touch 512 consecutive bytes (a chunk-contiguous layout would
+  // put all 32 lanes on the same four banks)
   float* xs = reinterpret_cast<float*>(sm_gu + (size_t)a.rmax * B1Row<D>::kGu);  // [D]
   __shared__ Seg seg[kMaxSeg];
   __shared__ int nseg_sh, nseg_all, n_rows, nsh_rows_s, top_idx[8];
@@ -355,8 +359,10 @@ __global__ void __launch_bounds__(kB1Threads, 1) experts_b1_kernel(B1Args a) {
       lo.z = __uint_as_float(u[1] << 16); lo.w = __uint_as_float(u[1] & 0xFFFF0000u);
       hi.x = __uint_as_float(u[2] << 16); hi.y = __uint_as_float(u[2] & 0xFFFF0000u);
       hi.z = __uint_as_float(u[3] << 16); hi.w = __uint_as_float(u[3] & 0xFFFF0000u);
-      reinterpret_cast<float4*>(xs)[2 * i] = lo;
-      reinterpret_cast<float4*>(xs)[2 * i + 1] = hi;
+      const int ch = i >> 2;                                              // 32-column chunk
+      const int slot = ((ch >> 5) * 8 + (i & 3) * 2) * 32 + (ch & 31);
+      reinterpret_cast<float4*>(xs)[slot] = lo;
+      reinterpret_cast<float4*>(xs)[slot + 32] = hi;
       m = fmaxf(m, fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(lo.z), fabsf(lo.w))));
       m = fmaxf(m, fmaxf(fmaxf(fabsf(hi.x), fabsf(hi.y)), fmaxf(fabsf(hi.z), fabsf(hi.w))));
     }
@@ -378,10 +384,10 @@ __global__ void __launch_bounds__(kB1Threads, 1) experts_b1_kernel(B1Args a) {
     const float sc = exp2i(shift);
 #pragma unroll
     for (int q = 0; q < CPL; ++q) {
-      const float4* xp = reinterpret_cast<const float4*>(xs + (lane + 32 * q) * 32);
+      const float4* xp = reinterpret_cast<const float4*>(xs) + q * 8 * 32 + lane;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 v = xp[i];
+        const float4 v = xp[i * 32];
         __half2 h0 = __floats2half2_rn(v.x * sc, v.y * sc), h1 = __floats2half2_rn(v.z * sc, v.w * sc);
         xh[q][2 * i] = *reinterpret_cast<uint32_t*>(&h0);
         xh[q][2 * i + 1] = *reinterpret_cast<uint32_t*>(&h1);
