@@ -33,8 +33,10 @@
 // held as f16 after an exact power-of-two prescale (max|x| mapped into
 // [2^14, 2^15)), and the products are accumulated in fp32 with the
 // mixed-precision FMA (f16 x f16 + f32): every product is exact, only the
-// fp32 sums round.  W_down is applied with f16 -> f32 weights against fp32 h.
+// fp32 sums round.  W_down is applied on the tensor cores (mma.sync, exact
+// f16 weights against h split into f16 hi + lo, fp32 accumulation).
 #include "internal.h"
+#include "mma_frag.cuh"
 #include "sm100.cuh"
 
 namespace nvmoe {
@@ -46,12 +48,7 @@ using namespace sm100;
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-__device__ __forceinline__ void cvt_e2m1x8(uint32_t w, uint32_t (&o)[4]) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
-}
+using frag::cvt_e2m1x8;
 
 // acc += lo(a) * lo(b) and acc2 += hi(a) * hi(b), f16 inputs, fp32 accumulate
 __device__ __forceinline__ void fma2_mixed(uint32_t a, uint32_t b, float& acc, float& acc2) {
@@ -60,23 +57,12 @@ __device__ __forceinline__ void fma2_mixed(uint32_t a, uint32_t b, float& acc, f
       : "+f"(acc), "+f"(acc2) : "r"(a), "r"(b));
 }
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
 // One L2 load that the compiler may neither repeat nor drop (a plain __ldcg
 // can be rematerialised inside later loops, re-paying the L2 latency each
 // time).  No memory clobber, so several of these stay in flight together.
 __device__ __forceinline__ float ld_once_f32(const float* p) {
   float v;
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ int ld_once_s32(const int32_t* p) {
-  int v;
-  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 
@@ -430,8 +416,16 @@ __global__ void __launch_bounds__(kB1Threads, 1) experts_b1_kernel(B1Args a) {
 // ---------------------------------------------------------------------------
 // down projection + combine: CTA owns kRD output rows, sums every slot
 // ---------------------------------------------------------------------------
-constexpr int kRD = 16;          // output rows per CTA (16 threads per row)
+// The 16 rows of a CTA are one MMA tile (m16n8k16): A = W_down rows (E2M1 code
+// times E4M3 block scale, exact in f16), B column 0 = hi and column 1 = lo of
+// h (f16 split after a per-slot power-of-two prescale), so every k step costs
+// one MMA and the products are exact.  The k range (slots x d_ff) is cut into
+// 128-wide chunks; warp w takes chunks w, w + 8, ... (two accumulators, so
+// the MMA chain of a chunk is four steps deep) and the eight warp sums are
+// added in a fixed order.
+constexpr int kRD = 16;          // output rows per CTA (one MMA tile)
 constexpr int kDThreads = 256;
+constexpr int kDWarps = kDThreads / 32;
 constexpr int kMaxSlots = 12;
 
 struct DnArgs {
@@ -445,18 +439,32 @@ struct DnArgs {
   int d, f, E, k, S, residual;
 };
 
+// shared-memory plan of down_b1 for NS slots (byte offsets)
+template <int F>
+struct DnB1Smem {
+  static constexpr int FB = F / 2, FS = F / 16;   // code / scale bytes per row
+  __host__ __device__ static size_t codes(int) { return 0; }  // [NS][kRD][FB]
+  __host__ __device__ static size_t scales(int ns) { return (size_t)ns * kRD * FB; }  // [NS][kRD][FS]
+  __host__ __device__ static size_t hi(int ns) { return scales(ns) + (size_t)ns * kRD * FS; }  // [NS][F] f16, k-permuted
+  __host__ __device__ static size_t lo(int ns) { return hi(ns) + (size_t)ns * F * 2; }  // [NS][F] f16, k-permuted
+  __host__ __device__ static size_t unshift(int ns) { return lo(ns) + (size_t)ns * F * 2; }  // [kMaxSlots] fp32
+  __host__ __device__ static size_t red(int ns) { return unshift(ns) + kMaxSlots * sizeof(float); }  // [kDWarps][kRD] fp32
+  __host__ __device__ static size_t total(int ns) { return red(ns) + kDWarps * kRD * sizeof(float); }
+};
+
 template <int F>
 __global__ void __launch_bounds__(kDThreads) down_b1_kernel(DnArgs a) {
-  constexpr int FB = F / 2, FS = F / 16;     // code / scale bytes per row
-  constexpr int EPL = F / 32;                 // elements per lane
+  static_assert(F % 128 == 0, "down_b1 works on 128-wide k chunks of d_ff");
+  using L = DnB1Smem<F>;
+  constexpr int FB = L::FB, FS = L::FS, NCH = F / 128;
   extern __shared__ __align__(128) uint8_t smem[];
   const int NS = a.k + a.S;
-  uint8_t* sc_codes = smem;                                     // [NS][kRD][FB]
-  uint8_t* sc_scales = sc_codes + (size_t)NS * kRD * FB;        // [NS][kRD][FS]
-  // h of every slot, 4 floats of padding after each 32 so that the 16 threads
-  // of a row (32 columns apart) hit distinct banks
-  constexpr int HP = F + F / 8;
-  float* hs = reinterpret_cast<float*>(sc_scales + (size_t)NS * kRD * FS);  // [NS][HP]
+  uint8_t* sc_codes = smem + L::codes(NS);
+  uint8_t* sc_scales = smem + L::scales(NS);
+  uint8_t* h_hi = smem + L::hi(NS);
+  uint8_t* h_lo = smem + L::lo(NS);
+  float* unshift = reinterpret_cast<float*>(smem + L::unshift(NS));
+  float* red = reinterpret_cast<float*>(smem + L::red(NS));
   __shared__ __align__(8) uint64_t bar;
   __shared__ int sel_idx[8];
   __shared__ float sel_w[8];
@@ -486,50 +494,76 @@ __global__ void __launch_bounds__(kDThreads) down_b1_kernel(DnArgs a) {
   }
   griddep_launch();
   griddep_wait();
-  // h of every slot (written by the experts kernel)
-  for (int i = threadIdx.x; i < NS * F / 4; i += kDThreads) {
-    const int s = i / (F / 4), c4 = i % (F / 4);   // c4 * 4 = column
-    reinterpret_cast<float4*>(hs + (size_t)s * HP + (c4 >> 3) * 36)[c4 & 7] =
-        __ldcg(reinterpret_cast<const float4*>(a.h) + i);
+  // h of every slot (written by the experts kernel) -> prescaled f16 hi + lo,
+  // k-permuted per 128 chunk; warp w converts slots w, w + 8
+  for (int s = warp; s < NS; s += kDWarps) {
+    const float4* src = reinterpret_cast<const float4*>(a.h + (size_t)s * F);
+    float4 v[F / 128];
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < F / 128; ++i) {
+      v[i] = __ldcg(src + lane + 32 * i);
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+    }
+    const int shift = frag::prescale_shift(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+    const float sc = frag::pow2i(shift);
+#pragma unroll
+    for (int i = 0; i < F / 128; ++i) {
+      const int k0 = 4 * (lane + 32 * i), kp = k0 % 128;
+      const size_t off = (size_t)s * F * 2 + (k0 / 128) * 256 + frag::perm_off(kp / 32, (kp % 32) / 4);
+      uint2 hi, lo;
+      frag::split_hi_lo(v[i].x * sc, v[i].y * sc, v[i].z * sc, v[i].w * sc, hi, lo);
+      *reinterpret_cast<uint2*>(h_hi + off) = hi;
+      *reinterpret_cast<uint2*>(h_lo + off) = lo;
+    }
+    if (lane == 0) unshift[s] = frag::pow2i(-shift);
   }
   __syncthreads();
   const bool ok = wait_parity(&bar, 0);
   if (!ok) latch_status(a.status, MOE_ERR_TIMEOUT);
-  // 16 threads per output row; thread q of a row covers columns [32q, 32q+32)
-  // of every slot: one 16-byte code load, two block scales, eight 16-byte h
-  // loads (shared by the rows, so broadcast) per slot
-  static_assert(F == 512, "down_b1 maps 16 threads x 32 columns onto d_ff = 512");
-  const int i = threadIdx.x >> 4, q = threadIdx.x & 15;
-  float acc = 0.f;
-  for (int s = 0; s < NS; ++s) {
-    const uint4 cw = *reinterpret_cast<const uint4*>(sc_codes + ((size_t)s * kRD + i) * FB + q * 16);
-    const uint32_t s2 = *reinterpret_cast<const uint16_t*>(sc_scales + ((size_t)s * kRD + i) * FS + q * 2);
-    const float4* hp = reinterpret_cast<const float4*>(hs + (size_t)s * HP + q * 36);
-    const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
-    float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+
+  // MMA lane roles: gq = lane / 4 is the A row (and B column), c = lane % 4
+  // the quad position; B columns 0 (hi) and 1 (lo) come from lanes 0..7.
+  const int gq = lane >> 2, c = lane & 3;
+  float y0 = 0.f, y8 = 0.f;
+  for (int u = warp; u < NS * NCH; u += kDWarps) {
+    const int s = u / NCH, ch = u - s * NCH;
+    const uint8_t* cg = sc_codes + ((size_t)s * kRD + gq) * FB + ch * 64 + c * 16;
+    const uint4 wg = *reinterpret_cast<const uint4*>(cg);
+    const uint4 wg8 = *reinterpret_cast<const uint4*>(cg + 8 * FB);
+    const uint8_t* sp = sc_scales + ((size_t)s * kRD + gq) * FS + ch * 8 + c * 2;
+    const uint32_t s2 = frag::cvt_e4m3x2_f16x2(*reinterpret_cast<const uint16_t*>(sp));
+    const uint32_t s28 = frag::cvt_e4m3x2_f16x2(*reinterpret_cast<const uint16_t*>(sp + 8 * FS));
+    const uint8_t* hb = (gq == 0 ? h_hi : h_lo) + (size_t)s * F * 2 + ch * 256;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      uint32_t o[4];
-      cvt_e2m1x8(ws[v], o);
-      const float4 h0 = hp[2 * v], h1 = hp[2 * v + 1];
-      const float2 w0 = f16x2_to_f32x2(o[0]), w1 = f16x2_to_f32x2(o[1]);
-      const float2 w2 = f16x2_to_f32x2(o[2]), w3 = f16x2_to_f32x2(o[3]);
-      float& blo = (v < 2) ? b0 : b2;
-      float& bhi = (v < 2) ? b1 : b3;
-      blo = fmaf(w0.x, h0.x, blo); bhi = fmaf(w0.y, h0.y, bhi);
-      blo = fmaf(w1.x, h0.z, blo); bhi = fmaf(w1.y, h0.w, bhi);
-      blo = fmaf(w2.x, h1.x, blo); bhi = fmaf(w2.y, h1.y, bhi);
-      blo = fmaf(w3.x, h1.z, blo); bhi = fmaf(w3.y, h1.w, bhi);
+    for (int wd = 0; wd < 4; ++wd) {
+      const uint32_t sg = wd < 2 ? frag::bcast_lo(s2) : frag::bcast_hi(s2);
+      const uint32_t sg8 = wd < 2 ? frag::bcast_lo(s28) : frag::bcast_hi(s28);
+      uint32_t afp[2][4];
+      frag::a_frag_pair(afp[0], afp[1], frag::word_of(wg, wd), frag::word_of(wg8, wd), sg, sg8);
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const uint2 b = gq < 2 ? frag::lds64(hb + frag::perm_off(c, 2 * wd + h2)) : make_uint2(0u, 0u);
+        frag::mma_f16(acc[h2], afp[h2], b.x, b.y);
+      }
     }
-    const float2 sc = e4m3x2_to_f32x2(s2);
-    acc = fmaf(b0 + b1, sc.x, acc);
-    acc = fmaf(b2 + b3, sc.y, acc);
+    // lanes with c == 0 hold columns 0 (hi) and 1 (lo) of rows gq and gq + 8
+    const float us = unshift[s];
+    y0 = fmaf((acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1]), us, y0);
+    y8 = fmaf((acc[0][2] + acc[0][3]) + (acc[1][2] + acc[1][3]), us, y8);
   }
-  acc = segment_sum(acc, 16);
-  if (q == 0) {
-    float y = acc;
-    if (a.residual) y += __bfloat162float(a.x[r0 + i]);
-    a.y[r0 + i] = __float2bfloat16_rn(y);
+  if (c == 0) {
+    red[warp * kRD + gq] = y0;
+    red[warp * kRD + gq + 8] = y8;
+  }
+  __syncthreads();
+  if (threadIdx.x < kRD) {
+    float y = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDWarps; ++w) y += red[w * kRD + threadIdx.x];
+    if (a.residual) y += __bfloat162float(a.x[r0 + threadIdx.x]);
+    a.y[r0 + threadIdx.x] = __float2bfloat16_rn(y);
   }
 }
 
@@ -574,8 +608,7 @@ bool b1_plan(const moe_config& c, int sm_count, int ctas_per_sm, int* grid, int*
 size_t b1_row_bytes(int d) { return (size_t)d + d / 8; }
 
 static size_t down_smem(const moe_config& c) {
-  const int NS = c.top_k + c.n_shared, F = c.d_ff;
-  return (size_t)NS * kRD * (F / 2 + F / 16) + (size_t)NS * (F + F / 8) * sizeof(float) + 64;
+  return DnB1Smem<512>::total(c.top_k + c.n_shared);   // b1_supported() requires d_ff = 512
 }
 
 // The three kernels of a token overlap through PDL only if an SM can hold an

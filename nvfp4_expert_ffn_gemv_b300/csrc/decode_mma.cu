@@ -36,10 +36,13 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "mma_frag.cuh"
 
 namespace nvmoe {
 
 namespace {
+
+using namespace frag;
 
 constexpr int kThreads = 256;   // 8 warps x 16 weight rows = 128 rows per tile
 constexpr int kTok = 8;         // tokens (positions) per tile: one MMA column group
@@ -48,86 +51,12 @@ constexpr int kChunk = 128;     // k per chunk
 // ---------------------------------------------------------------------------
 // small helpers
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
-  uint32_t out;
-  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(out) : "r"(byte));
-  return out;
-}
-
-__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two) {
-  uint32_t out;
-  const uint16_t in = static_cast<uint16_t>(two & 0xFFFF);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(in));
-  return out;
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t out;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out) : "r"(a), "r"(b));
-  return out;
-}
-
-// {lo, lo} and {hi, hi} of an f16x2
-__device__ __forceinline__ uint32_t bcast_lo(uint32_t v) { return __byte_perm(v, v, 0x1010); }
-__device__ __forceinline__ uint32_t bcast_hi(uint32_t v) { return __byte_perm(v, v, 0x3232); }
-
-__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
-
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(s), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-
-// 2^k as a float for -126 <= k <= 127
-__device__ __forceinline__ float pow2i(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
-
-// exponent shift that maps max|v| (as fp32 bits, non-negative) into [2^14, 2^15)
-__device__ __forceinline__ int prescale_shift(uint32_t amax_bits) {
-  if (amax_bits == 0u) return 0;
-  const int ex = (int)((amax_bits >> 23) & 0xFF) - 127;
-  return max(-126, min(126, 14 - ex));
-}
-
-// byte offset, inside one 128-wide k chunk of f16 values, of the 4 values
-// k = 32c + 4kk + 0..3
-__device__ __forceinline__ int perm_off(int c, int kk) { return (kk * 4 + c) * 8; }
-
-// Eight E2M1 codes (one word, element 2j in the low nibble of byte j) -> four
-// exact f16x2, one mov splitting the word into bytes and four hardware cvts.
-__device__ __forceinline__ void cvt_e2m1x8(uint32_t w, uint32_t (&o)[4]) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
-}
-
-// A fragments of the two MMA steps 2w and 2w+1 from word w of the quad's code
-// slice of rows g (wg) and g+8 (wg8): bytes 0, 1 feed step 2w, bytes 2, 3 step
-// 2w+1; every f16x2 is multiplied by its row's block scale (exact).
-__device__ __forceinline__ void a_frag_pair(uint32_t (&a0)[4], uint32_t (&a1)[4], uint32_t wg, uint32_t wg8,
-                                            uint32_t sg, uint32_t sg8) {
-  uint32_t g[4], h[4];
-  cvt_e2m1x8(wg, g);
-  cvt_e2m1x8(wg8, h);
-  a0[0] = hmul2(g[0], sg);
-  a0[2] = hmul2(g[1], sg);
-  a0[1] = hmul2(h[0], sg8);
-  a0[3] = hmul2(h[1], sg8);
-  a1[0] = hmul2(g[2], sg);
-  a1[2] = hmul2(g[3], sg);
-  a1[1] = hmul2(h[2], sg8);
-  a1[3] = hmul2(h[3], sg8);
 }
 
 // Weight bytes are read once per call: a read-only load that does not allocate
@@ -137,10 +66,6 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
 struct MmaArgs {
