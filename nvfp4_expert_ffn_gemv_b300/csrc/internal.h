@@ -79,6 +79,7 @@ namespace nvmoe {
 
 cudaError_t launch_router(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
 cudaError_t launch_bucket(const moe_ctx* c, int T, cudaStream_t s);
+int bucket_kernel_count(int T);   // kernels launch_bucket() issues for T tokens
 cudaError_t prepare_bucket_kernel();
 cudaError_t launch_gateup_decode(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
 cudaError_t launch_down_decode(const moe_ctx* c, int T, cudaStream_t s);

@@ -447,9 +447,10 @@ moe_status moe_get_device_status(moe_ctx* x) {
 int moe_kernels_per_forward(moe_ctx* x, int T, int prefill) {
   if (!x || T <= 0) return 0;
   if (!prefill && T == 1 && x->b1_enabled) return 3;
-  if (prefill) return 8;   // router x2, bucket, quantise x, gather x, GEMM x2, combine
-  if (x->mma_enabled) return 7;   // router x2, bucket, x prescale, gate/up, down, combine
-  return 6;
+  const int nb = bucket_kernel_count(T);
+  if (prefill) return 7 + nb;   // router x2, bucketing, quantise x, gather x, GEMM x2, combine
+  if (x->mma_enabled) return 6 + nb;   // router x2, bucketing, x prescale, gate/up, down, combine
+  return 5 + nb;
 }
 
 }  // extern "C"

@@ -180,53 +180,61 @@ __global__ void __launch_bounds__(kStagedThreads, 1) router_partial_staged_kerne
   }
 }
 
-// a beats b: larger value first, NaN counts as -inf, ties to the lower index
-__device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
-  const float a = (va != va) ? -INFINITY : va;
-  const float b = (vb != vb) ? -INFINITY : vb;
-  return a > b || (a == b && ia < ib);
-}
-
-// k rounds of warp argmax over the (up to) 256 logits v[i] of expert lane + 32 i;
-// lane 0 writes idx and the renormalised softmax weights of token t.
+// k rounds of warp argmax over the (up to) 256 logits v[i] of expert lane + 32 i
+// (larger value first, ties to the lower expert, NaN below every number);
+// lanes j < K write idx and the renormalised softmax weight of token t's
+// choice j.  Each value maps to an order-preserving unsigned key, so a round
+// is a lane-local 8-way argmax, one warp max of the keys and one warp min of
+// the expert index among the lanes that hold the maximum.
 __device__ __forceinline__ void warp_select(const float (&v)[8], int E, int K, int t, int32_t* __restrict__ idx,
                                             float* __restrict__ wout, int* status) {
   const int lane = threadIdx.x & 31;
-  bool taken[8];
+  uint32_t key[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) taken[i] = lane + 32 * i >= E;
-  float sel_v[8];
-  int sel_e[8];
-  for (int j = 0; j < K; ++j) {
-    float bv = 0.f;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int ee = lane + 32 * i;
-      if (!taken[i] && (be == 0x7fffffff || beats(v[i], ee, bv, be))) { bv = v[i]; be = ee; }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (oe != 0x7fffffff && (be == 0x7fffffff || beats(ov, oe, bv, be))) { bv = ov; be = oe; }
-    }
-    sel_v[j] = bv;
-    sel_e[j] = be;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (lane + 32 * i == be) taken[i] = true;
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t u = __float_as_uint(v[i]);
+    uint32_t kk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    if (v[i] != v[i]) kk = 1u;
+    key[i] = lane + 32 * i < E ? max(kk, 1u) : 0u;   // 0: no expert
   }
-  if (lane == 0) {
-    const float m = sel_v[0];
-    float z[8], sum = 0.f;
-    for (int j = 0; j < K; ++j) { z[j] = __expf(sel_v[j] - m); sum += z[j]; }
-    for (int j = 0; j < K; ++j) {
-      int ee = sel_e[j];
-      if (ee < 0 || ee >= E) { latch_status(status, MOE_ERR_DEVICE_CHECK); ee = 0; }
-      idx[(size_t)t * K + j] = ee;
-      wout[(size_t)t * K + j] = z[j] / sum;
+  float my_v = 0.f;
+  uint32_t my_e = 0u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < K) {
+      uint32_t k01 = key[1] > key[0] ? key[1] : key[0]; int i01 = key[1] > key[0] ? 1 : 0;
+      uint32_t k23 = key[3] > key[2] ? key[3] : key[2]; int i23 = key[3] > key[2] ? 3 : 2;
+      uint32_t k45 = key[5] > key[4] ? key[5] : key[4]; int i45 = key[5] > key[4] ? 5 : 4;
+      uint32_t k67 = key[7] > key[6] ? key[7] : key[6]; int i67 = key[7] > key[6] ? 7 : 6;
+      uint32_t ka = k23 > k01 ? k23 : k01; int ia = k23 > k01 ? i23 : i01;
+      uint32_t kb = k67 > k45 ? k67 : k45; int ib = k67 > k45 ? i67 : i45;
+      const uint32_t best = kb > ka ? kb : ka;
+      const int bi = kb > ka ? ib : ia;
+      const uint32_t top = __reduce_max_sync(0xffffffffu, best);
+      const uint32_t win =
+          __reduce_min_sync(0xffffffffu, (best == top && top != 0) ? (uint32_t)(lane + 32 * bi) : 0xFFFFu);
+      float bv = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (i == bi) bv = v[i];
+        if (lane + 32 * i == (int)win) key[i] = 0;
+      }
+      const float sv = __shfl_sync(0xffffffffu, bv, (int)(win & 31));
+      if (lane == j) { my_v = sv; my_e = win; }
     }
+  }
+  // softmax over the chosen logits, one per lane (lane 0 holds the largest)
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);
+  const float z = lane < K ? expf(my_v - m) : 0.f;
+  float sum = z;
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);   // K <= 8 lanes
+  sum = __shfl_sync(0xffffffffu, sum, 0);
+  if (lane < K) {
+    int ee = (int)my_e;
+    if (ee >= E) { latch_status(status, MOE_ERR_DEVICE_CHECK); ee = 0; }
+    idx[(size_t)t * K + lane] = ee;
+    wout[(size_t)t * K + lane] = z / sum;
   }
 }
 

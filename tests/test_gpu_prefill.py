@@ -158,6 +158,30 @@ def test_prefill_small(lib, T):
         lib.moe_destroy(layer.ctx)
 
 
+@pytest.mark.parametrize("T", [1024, 1500])
+def test_bucketing_grid_path(lib, T):
+    """From 1024 tokens the bucketing runs as three grids (count, scan, scatter):
+    the per-expert counts equal the histogram of the chosen experts, and the
+    prefill output, which reads every position the scatter wrote, matches the
+    oracle on sampled tokens (T = 1500 leaves a ragged last chunk)."""
+    layer = harness.make_layer(lib, SMALL, seed=21, router_seed=22, fmt=0, max_tokens=2048)
+    try:
+        k, E = SMALL.top_k, SMALL.n_experts
+        xb, x = synth.tokens(SMALL, T, seed=400 + T)
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        counts = torch.empty((E,), dtype=torch.int32, device="cuda")
+        lib.moe_route(layer.ctx, xb.cuda(), T, idx, w, counts)
+        torch.cuda.synchronize()
+        assert lib.moe_get_device_status(layer.ctx) == 0
+        hist = np.bincount(idx.cpu().numpy().ravel(), minlength=E)
+        assert np.array_equal(counts.cpu().numpy(), hist)
+        sample = [0, 1, T // 2, T - 1] + list(range(5, T, 97))
+        _check_prefill(lib, layer, xb.cuda(), x.double().numpy(), T, sample=sample)
+    finally:
+        lib.moe_destroy(layer.ctx)
+
+
 def test_prefill_flint_4096_sampled(lib):
     s = synth.FLINT
     layer = harness.make_layer(lib, s, seed=synth.layer_seed(0), router_seed=synth.router_seed(0), fmt=0,
