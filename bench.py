@@ -63,34 +63,44 @@ WORKLOADS = {
 }
 
 
-def _kernel_sources_digest():
-    """sha256 over the CUDA kernel sources (the host-side ABI file excluded)."""
+#: CUDA sources whose kernels each workload's roofline covers (every header they include)
+TRAFFIC_SOURCES = {
+    "decode_b1": ("decode_b1.cu", "mma_frag.cuh", "sm100.cuh", "internal.h", "common.cuh"),
+    "stack": ("decode_b1.cu", "mma_frag.cuh", "sm100.cuh", "internal.h", "common.cuh"),
+    "decode_b64": ("decode_mma.cu", "mma_frag.cuh", "internal.h", "common.cuh"),
+    "prefill": ("prefill.cu", "sm100.cuh", "internal.h", "common.cuh"),
+    "prefill_32k": ("prefill.cu", "sm100.cuh", "internal.h", "common.cuh"),
+}
+
+
+def _sources_digest(names):
+    """sha256 over the named files of the package's csrc directory, in the given order."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "nvfp4_expert_ffn_gemv_b300", "csrc")
-    for n in sorted(os.listdir(d)):
-        if n.endswith((".cu", ".cuh")) and n != "moe_abi.cu":
-            h.update(n.encode())
-            with open(os.path.join(d, n), "rb") as fh:
-                h.update(fh.read())
+    for n in names:
+        h.update(n.encode())
+        with open(os.path.join(d, n), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()
 
 
 def _traffic(workload):
-    """DRAM bytes per launch from profiles/traffic.txt, or None when the kernels changed since."""
+    """DRAM bytes per launch from profiles/traffic.txt, or None once the workload's kernel
+    sources differ from the ones the counters were taken on."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.txt")) as fh:
             lines = [ln.strip() for ln in fh if ln.strip() and not ln.startswith("#")]
     except OSError:
         return None
-    kv = dict(ln.split("=", 1) for ln in lines if ln.startswith("sources_sha256="))
-    if kv.get("sources_sha256") != _kernel_sources_digest():
-        return None
     for ln in lines:
-        if ln.split(" ", 1)[0] == workload:
-            for tok in ln.split():
-                if tok.startswith("traffic_bytes="):
-                    return int(tok.split("=", 1)[1])
+        toks = ln.split()
+        if toks[0] != workload:
+            continue
+        kv = dict(t.split("=", 1) for t in toks[1:] if "=" in t)
+        if workload not in TRAFFIC_SOURCES or kv.get("sha256") != _sources_digest(TRAFFIC_SOURCES[workload]):
+            return None
+        return int(kv["traffic_bytes"]) if "traffic_bytes" in kv else None
     return None
 
 
