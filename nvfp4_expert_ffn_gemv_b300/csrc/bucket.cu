@@ -215,42 +215,58 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T
 
 // ---------------------------------------------------------------------------
 // Large batches: the same four phases as three grids, so that phases A and D
-// run on every SM instead of one.
-//   count:   one warp per 32-token chunk (phase A) -> rank, chunk_cnt
-//   scan:    one block; four threads per expert prefix the chunk counts
+// run on every SM instead of one.  Chunks of 32 tokens are grouped by 8
+// (256 tokens):
+//   count:   one block per group, one warp per chunk (phase A) -> rank; the
+//            block also prefixes its 8 chunk counts per expert (chunk_cnt,
+//            relative to the group) and writes the group totals (group_cnt)
+//   scan:    one block; four threads per expert prefix the group totals
 //            (phase B), then warp 0 runs phase C
 //   scatter: one thread per (token, choice) pair (phase D)
 // ---------------------------------------------------------------------------
-constexpr int kCountWarps = 2;
+constexpr int kGroupChunks = 8;                      // chunks per group = warps per count block
 constexpr int kScanThreads = 1024;
 constexpr int kScanParts = kScanThreads / kMaxE;   // threads per expert
 constexpr int kScanBatch = 32;                       // loads in flight per thread
 
-__global__ void __launch_bounds__(kCountWarps * 32) bucket_count_kernel(Routing r, int T, int k, int E,
-                                                                        int* status) {
-  __shared__ uint32_t mask[kCountWarps][kMaxE];
+__global__ void __launch_bounds__(kGroupChunks * 32) bucket_count_kernel(Routing r, int T, int k, int E,
+                                                                         int* status) {
+  __shared__ uint32_t mask[kGroupChunks][kMaxE];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x * kCountWarps + warp;
-  if (c >= (T + 31) / 32) return;
+  const int nchunks = (T + 31) / 32;
+  const int g = blockIdx.x, c = g * kGroupChunks + warp;
   for (int e = lane; e < E; e += 32) mask[warp][e] = 0u;
   __syncwarp();
-  const int t = c * 32 + lane;
-  const bool valid = t < T;
-  int ej[8];
-  if (valid) {
-    for (int j = 0; j < k; ++j) {
-      int e = __ldg(r.idx + (size_t)t * k + j);
-      if (e < 0 || e >= E) { latch_status(status, MOE_ERR_DEVICE_CHECK); e = 0; }
-      ej[j] = e;
-      atomicOr(&mask[warp][e], 1u << lane);
+  if (c < nchunks) {
+    const int t = c * 32 + lane;
+    const bool valid = t < T;
+    int ej[8];
+    if (valid) {
+      for (int j = 0; j < k; ++j) {
+        int e = __ldg(r.idx + (size_t)t * k + j);
+        if (e < 0 || e >= E) { latch_status(status, MOE_ERR_DEVICE_CHECK); e = 0; }
+        ej[j] = e;
+        atomicOr(&mask[warp][e], 1u << lane);
+      }
+    }
+    __syncwarp();
+    if (valid) {
+      const uint32_t lower = (1u << lane) - 1u;
+      for (int j = 0; j < k; ++j) r.rank[(size_t)t * k + j] = __popc(mask[warp][ej[j]] & lower);
     }
   }
-  __syncwarp();
-  if (valid) {
-    const uint32_t lower = (1u << lane) - 1u;
-    for (int j = 0; j < k; ++j) r.rank[(size_t)t * k + j] = __popc(mask[warp][ej[j]] & lower);
+  __syncthreads();
+  // per expert: each chunk's count prefix inside the group, and the group total
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kGroupChunks; ++w) {
+      const int cc = g * kGroupChunks + w;
+      if (cc >= nchunks) break;
+      r.chunk_cnt[(size_t)cc * E + e] = run;
+      run += __popc(mask[w][e]);
+    }
+    r.group_cnt[(size_t)g * E + e] = run;
   }
-  for (int e = lane; e < E; e += 32) r.chunk_cnt[(size_t)c * E + e] = __popc(mask[warp][e]);
 }
 
 __global__ void __launch_bounds__(kScanThreads) bucket_scan_kernel(Routing r, int T, int k, int E, int S,
@@ -259,33 +275,33 @@ __global__ void __launch_bounds__(kScanThreads) bucket_scan_kernel(Routing r, in
   __shared__ int cnt[kMaxE];
   __shared__ int off[kMaxE + 1];
   const int e = threadIdx.x % kMaxE, q = threadIdx.x / kMaxE;
-  const int nchunks = (T + 31) / 32;
-  const int per = (nchunks + kScanParts - 1) / kScanParts;
-  const int c0 = min(nchunks, q * per), c1 = min(nchunks, c0 + per);
-  // B1. this thread's share of expert e's chunk counts
+  const int ngroups = ((T + 31) / 32 + kGroupChunks - 1) / kGroupChunks;
+  const int per = (ngroups + kScanParts - 1) / kScanParts;
+  const int g0 = min(ngroups, q * per), g1 = min(ngroups, g0 + per);
+  // B1. this thread's share of expert e's group totals
   int sum = 0;
   if (e < E) {
-    for (int cb = c0; cb < c1; cb += kScanBatch) {
+    for (int gb = g0; gb < g1; gb += kScanBatch) {
       int v[kScanBatch];
 #pragma unroll
-      for (int i = 0; i < kScanBatch; ++i) v[i] = cb + i < c1 ? __ldcg(r.chunk_cnt + (size_t)(cb + i) * E + e) : 0;
+      for (int i = 0; i < kScanBatch; ++i) v[i] = gb + i < g1 ? __ldcg(r.group_cnt + (size_t)(gb + i) * E + e) : 0;
 #pragma unroll
       for (int i = 0; i < kScanBatch; ++i) sum += v[i];
     }
   }
   part[q][e] = sum;
   __syncthreads();
-  // B2. exclusive prefix over the chunks, in chunk order
+  // B2. exclusive prefix over the groups, in group order
   if (e < E) {
     int run = 0;
     for (int qq = 0; qq < q; ++qq) run += part[qq][e];
-    for (int cb = c0; cb < c1; cb += kScanBatch) {
+    for (int gb = g0; gb < g1; gb += kScanBatch) {
       int v[kScanBatch];
 #pragma unroll
-      for (int i = 0; i < kScanBatch; ++i) v[i] = cb + i < c1 ? __ldcg(r.chunk_cnt + (size_t)(cb + i) * E + e) : 0;
+      for (int i = 0; i < kScanBatch; ++i) v[i] = gb + i < g1 ? __ldcg(r.group_cnt + (size_t)(gb + i) * E + e) : 0;
 #pragma unroll
       for (int i = 0; i < kScanBatch; ++i) {
-        if (cb + i < c1) r.chunk_cnt[(size_t)(cb + i) * E + e] = run;
+        if (gb + i < g1) r.group_cnt[(size_t)(gb + i) * E + e] = run;
         run += v[i];
       }
     }
@@ -301,7 +317,8 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(Routing r, int T, i
     const int t = s / k;
     int e = __ldg(r.idx + s);
     if (e < 0 || e >= E) e = 0;   // reported by the count kernel
-    const int p = __ldg(r.offsets + e) + __ldg(r.chunk_cnt + (size_t)(t >> 5) * E + e) + __ldg(r.rank + s);
+    const int p = __ldg(r.offsets + e) + __ldg(r.group_cnt + (size_t)(t >> 8) * E + e) +
+                  __ldg(r.chunk_cnt + (size_t)(t >> 5) * E + e) + __ldg(r.rank + s);
     r.slot_pos[s] = p;
     r.pos_tok[p] = t;
   } else if (s < T * k + S * T) {
@@ -328,9 +345,8 @@ int bucket_kernel_count(int T) { return T >= kBucketGridTokens ? 3 : 1; }
 cudaError_t launch_bucket(const moe_ctx* c, int T, cudaStream_t s) {
   const int k = c->cfg.top_k, E = c->cfg.n_experts, S = c->cfg.n_shared;
   if (T >= kBucketGridTokens) {
-    const int nchunks = (T + 31) / 32;
-    bucket_count_kernel<<<(nchunks + kCountWarps - 1) / kCountWarps, kCountWarps * 32, 0, s>>>(c->r, T, k, E,
-                                                                                               c->status);
+    const int ngroups = (T + 32 * kGroupChunks - 1) / (32 * kGroupChunks);
+    bucket_count_kernel<<<ngroups, kGroupChunks * 32, 0, s>>>(c->r, T, k, E, c->status);
     bucket_scan_kernel<<<1, kScanThreads, 0, s>>>(c->r, T, k, E, S, c->status);
     const int n = T * k + S * T;
     bucket_scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(c->r, T, k, E, S);

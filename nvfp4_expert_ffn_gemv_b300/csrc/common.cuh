@@ -131,6 +131,7 @@ struct Routing {
   int32_t* act_ppos;   // [E+S+1] prefill: padded first row (multiple of 128), total last
   int32_t* blk_a;      // [padded rows / 128] prefill: active expert of each 128-row block
   int32_t* chunk_cnt;  // [ceil(T/32)][E] scratch
+  int32_t* group_cnt;  // [ceil(T/256)][E] scratch (bucketing of large batches)
   int32_t* rank;       // [T*k] scratch
 };
 

@@ -74,6 +74,7 @@ size_t carve(moe_ctx* x, uint8_t* base) {
   x->r.act_ppos = cv.take<int32_t>(base, E + S + 1);
   x->r.blk_a = cv.take<int32_t>(base, (T * (k + S) + 127) / 128 + E + S);
   x->r.chunk_cnt = cv.take<int32_t>(base, ((T + 31) / 32) * E);
+  x->r.group_cnt = cv.take<int32_t>(base, ((T + 255) / 256) * E);
   x->r.rank = cv.take<int32_t>(base, T * k);
   x->h = cv.take<float>(base, P * f);
   x->yexp = cv.take<float>(base, P * d);
