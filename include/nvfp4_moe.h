@@ -187,7 +187,9 @@ MOE_API moe_status moe_set_profile_events(moe_ctx* ctx, cudaEvent_t start, cudaE
  * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK), then clear it. */
 MOE_API moe_status moe_get_device_status(moe_ctx* ctx);
 
-/* Number of kernels one forward call launches for T tokens (for accounting). */
+/* Number of kernels one forward call launches for T tokens (for accounting):
+ * 3 for batch-1 decode; otherwise the router (2), bucketing (1 kernel below
+ * 1024 tokens, 3 from 1024 on) and the path's expert and combine kernels. */
 MOE_API int moe_kernels_per_forward(moe_ctx* ctx, int T, int prefill);
 
 /* Free everything the context owns.  NULL is accepted. */
