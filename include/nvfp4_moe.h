@@ -67,6 +67,13 @@ typedef enum {
 
 typedef enum { MOE_W_NVFP4 = 0, MOE_W_BF16 = 1 } moe_weight_format;
 
+/* Debug flags of moe_set_debug. */
+enum {
+  MOE_DEBUG_KEEP_LOGITS = 1,   /* routing stores the fp32 logits it ranked (moe_debug_logits) */
+  MOE_DEBUG_FORCE_TIMEOUT = 2  /* kernels with bounded waits report MOE_ERR_TIMEOUT after their
+                                  waits have completed normally (tests the status plumbing) */
+};
+
 typedef struct {
   int d_model;        /* hidden size: 256, 512, 1024, 2048 or 4096               */
   int n_experts;      /* routed experts, 1..256                                  */
@@ -98,14 +105,25 @@ typedef struct {
 
 /* Validate the config, allocate the device arena on `device`, copy and
  * repack the weights into the library's device layouts, allocate scratch for
- * max_tokens.  On success *out owns all of it until moe_destroy. */
+ * max_tokens.  On success *out owns all of it until moe_destroy.
+ * Pages: the layer's shape (256 routed experts, 6 per token, one shared
+ * expert, NVFP4 weights) is the OrcaRouter page's, sections
+ * "このアーキテクチャはメモリ帯域幅に関する主張である" and
+ * "量子化のレシピは最も転用しやすい部分です"; sizes are configurable.
+ * Errors: MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED on the host before any
+ * allocation, MOE_ERR_OOM when the arena cannot be allocated (nothing is
+ * left allocated), MOE_ERR_CUDA if a copy or set-up kernel fails. */
 MOE_API moe_status moe_init(const moe_config* cfg, const moe_weights* weights, int device,
                     moe_ctx** out);
 
 /* Router only: logits, top-k, combine weights and per-expert token counts.
  * x [T][d_model] bf16 -> idx [T][top_k] int32, w [T][top_k] fp32,
- * counts [n_experts] int32 (any of the three outputs may be NULL).
- * 0 <= T <= max_tokens. */
+ * counts [n_experts] int32 (any of the three outputs may be NULL), all
+ * device pointers owned by the caller.  0 <= T <= max_tokens.
+ * Pages: "6 of 256 experts per token" (OrcaRouter page, section
+ * "このアーキテクチャはメモリ帯域幅に関する主張である"); the scoring function
+ * (fp32 logits, top-k with ties to the lower expert, softmax renormalised over
+ * the chosen k) is this library's reading, stated at the top of this file. */
 MOE_API moe_status moe_route(moe_ctx* ctx, const void* x_bf16, int T, int32_t* idx, float* w,
                      int32_t* counts, cudaStream_t stream);
 
@@ -121,7 +139,7 @@ MOE_API moe_status moe_route(moe_ctx* ctx, const void* x_bf16, int T, int32_t* i
  *   router      [d_model][n_experts] fp32, device;  router_bias [n_experts] fp32
  *               device, or NULL for none
  *   idx, w      [T][top_k] int32 / fp32 outputs, device, both required
- *   d_model a multiple of 256 in 256..8192, 1 <= n_experts <= 256,
+ *   d_model a multiple of 256 in 256..4096, 1 <= n_experts <= 256,
  *   1 <= top_k <= min(8, n_experts); T == 0 does nothing.  A pointer the GPU
  *   cannot dereference (plain pageable host memory) is MOE_ERR_INVALID_ARG.
  *
@@ -136,24 +154,36 @@ MOE_API moe_status moe_route(moe_ctx* ctx, const void* x_bf16, int T, int32_t* i
  * shared-memory limit is raised (cudaFuncSetAttribute); make that first call
  * outside any stream capture.  Calls are asynchronous on `stream`; two calls that can
  * run on the GPU at the same time (different streams, different host threads)
- * share the one array and race -- order them on one stream or with events. */
+ * share the one array and race -- order them on one stream or with events.
+ * Having no context, it has no device status word either: the device-side
+ * consistency checks that moe_route reports through moe_get_device_status
+ * are not reported by this entry point. */
 MOE_API moe_status moe_route_noalloc(const void* x_bf16, int T, const float* router,
                              const float* router_bias, int d_model, int n_experts, int top_k,
                              int32_t* idx, float* w, cudaStream_t stream);
 
 /* Decode form of the layer: activations stay exact (bf16 -> fp32), the NVFP4
  * weights are dequantised on the fly.  y [T][d_model] bf16 (may not alias x).
- * If `residual` is non-zero, y = bf16(x + layer(x)) (the stack's residual). */
+ * If `residual` is non-zero, y = bf16(x + layer(x)) (the stack's residual).
+ * x and y are caller-owned device buffers, 16-byte aligned.
+ * Pages: decode as moving each chosen weight from memory to the ALUs
+ * (OrcaRouter page, section "このアーキテクチャはメモリ帯域幅に関する主張である"). */
 MOE_API moe_status moe_forward_decode(moe_ctx* ctx, const void* x_bf16, int T, void* y_bf16,
                               int residual, cudaStream_t stream);
 
 /* Prefill form: x and the SwiGLU output h are quantised to NVFP4 (16-element
  * E4M3 block scales, tensor scale 1) and every expert product runs as a
- * block-scaled FP4 x FP4 tensor-core GEMM.  NVFP4 weights only. */
+ * block-scaled FP4 x FP4 tensor-core GEMM.  NVFP4 weights only
+ * (MOE_ERR_UNSUPPORTED otherwise).  Buffers as for moe_forward_decode.
+ * Pages: the vendor lists "prompt processing" kernels among its custom
+ * kernels (OrcaRouter page, section "量子化のレシピは最も転用しやすい部分です"). */
 MOE_API moe_status moe_forward_prefill(moe_ctx* ctx, const void* x_bf16, int T, void* y_bf16,
                                int residual, cudaStream_t stream);
 
-/* Quantise n fp32 tensors w [n][rows][K] to canonical NVFP4 on the device:
+/* Pages: weights ship as NVFP4 (OrcaRouter page, section
+ * "量子化のレシピは最も転用しやすい部分です"); the rules below are this
+ * library's reading of the format.
+ * Quantise n fp32 tensors w [n][rows][K] to canonical NVFP4 on the device:
  * codes [n][rows][K/2], scales [n][rows][K/16], ts [n].  Rules (all fp32,
  * round-to-nearest-even):  ts = amax/2688;  s = E4M3(amax_16 / (6*ts));
  * q = E2M1(v / (e4m3(s)*ts)); zero tensors give ts = 0 and zero codes.
@@ -182,6 +212,30 @@ MOE_API moe_status moe_debug_routing(moe_ctx* ctx, int T, int32_t* idx, float* w
  * are external event records, so inside a stream capture they become event
  * record nodes of the graph and can be timed after a replay. */
 MOE_API moe_status moe_set_profile_events(moe_ctx* ctx, cudaEvent_t start, cudaEvent_t stop);
+
+/* Debugging: set the context's debug flags (MOE_DEBUG_*; 0 clears them).
+ * They apply to calls queued afterwards.  The pages have no counterpart. */
+MOE_API moe_status moe_set_debug(moe_ctx* ctx, int flags);
+
+/* Debugging: copy the fp32 logits the last routing ranked, logits
+ * [T][n_experts] (device pointer), T = that call's T.  Available after a
+ * batch-1 decode always, after other calls only if MOE_DEBUG_KEEP_LOGITS was
+ * set when they were queued; MOE_ERR_INVALID_ARG otherwise.  Asynchronous on
+ * `stream`.  The pages have no counterpart. */
+MOE_API moe_status moe_debug_logits(moe_ctx* ctx, int T, float* logits, cudaStream_t stream);
+
+/* Debugging: run the bounded device-side wait on an mbarrier that nothing
+ * ever arrives on and nothing copies to, giving up after spin_limit polls
+ * (>= 1).  The wait runs out and MOE_ERR_TIMEOUT is latched in the context's
+ * status word, as when a product kernel's copy never lands; no asynchronous
+ * operation is in flight, so the context stays usable.  The pages have no
+ * counterpart. */
+MOE_API moe_status moe_debug_wait_selftest(moe_ctx* ctx, int spin_limit, cudaStream_t stream);
+
+/* Testing: make the n-th device allocation the library performs from now on
+ * (the arena of a later moe_init) fail as if the device were out of memory;
+ * 0 disables.  Process-wide.  The pages have no counterpart. */
+MOE_API moe_status moe_debug_fail_alloc(int n);
 
 /* Synchronise the context's device and return the latched device status
  * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK), then clear it. */

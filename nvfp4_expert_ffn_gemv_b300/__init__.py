@@ -27,8 +27,11 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 #: every symbol the C header declares
 EXPORTS = ("moe_init", "moe_route", "moe_route_noalloc", "moe_forward_decode", "moe_forward_prefill", "moe_quantize_nvfp4",
-           "moe_debug_prefill_h", "moe_debug_routing", "moe_set_profile_events", "moe_get_device_status",
+           "moe_debug_prefill_h", "moe_debug_routing", "moe_set_profile_events", "moe_set_debug", "moe_debug_logits",
+           "moe_debug_wait_selftest", "moe_debug_fail_alloc", "moe_get_device_status",
            "moe_kernels_per_forward", "moe_destroy", "moe_status_string")
+MOE_DEBUG_KEEP_LOGITS = 1
+MOE_DEBUG_FORCE_TIMEOUT = 2
 
 
 class MoEError(RuntimeError):
@@ -70,6 +73,10 @@ def _load():
         "moe_debug_prefill_h": (i, [vp, i, vp, vp, vp]),
         "moe_debug_routing": (i, [vp, i, vp, vp, vp]),
         "moe_set_profile_events": (i, [vp, vp, vp]),
+        "moe_set_debug": (i, [vp, i]),
+        "moe_debug_logits": (i, [vp, i, vp, vp]),
+        "moe_debug_wait_selftest": (i, [vp, i, vp]),
+        "moe_debug_fail_alloc": (i, [i]),
         "moe_get_device_status": (i, [vp]),
         "moe_kernels_per_forward": (i, [vp, i, i]),
         "moe_destroy": (i, [vp]),
@@ -174,6 +181,22 @@ def moe_debug_routing(ctx, T: int, idx, w, stream=None) -> None:
 def moe_set_profile_events(ctx, start=None, stop=None) -> None:
     ev = lambda e: None if e is None else (e if isinstance(e, int) else e.cuda_event)  # noqa: E731
     _check("moe_set_profile_events", _lib.moe_set_profile_events(ctx, ev(start), ev(stop)))
+
+
+def moe_set_debug(ctx, flags: int) -> None:
+    _check("moe_set_debug", _lib.moe_set_debug(ctx, int(flags)))
+
+
+def moe_debug_logits(ctx, T: int, logits, stream=None) -> None:
+    _check("moe_debug_logits", _lib.moe_debug_logits(ctx, int(T), _ptr(logits), _stream(stream)))
+
+
+def moe_debug_wait_selftest(ctx, spin_limit: int, stream=None) -> None:
+    _check("moe_debug_wait_selftest", _lib.moe_debug_wait_selftest(ctx, int(spin_limit), _stream(stream)))
+
+
+def moe_debug_fail_alloc(n: int) -> None:
+    _check("moe_debug_fail_alloc", _lib.moe_debug_fail_alloc(int(n)))
 
 
 def moe_get_device_status(ctx) -> int:

@@ -69,7 +69,8 @@ __device__ __forceinline__ float ld_once_f32(const float* p) {
 // 2^k as a float for -126 <= k <= 127
 __device__ __forceinline__ float exp2i(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
 
-// top-k over E <= 256 logits by one warp; ties to the lower expert, NaN lowest.
+// top-k over E <= 256 logits by one warp; equal values (+0 and -0 included) to
+// the lower expert, NaN lowest.
 // Only compile-time register indices, so nothing spills to local memory.
 __device__ __forceinline__ void warp_topk(const float* logits, int E, int k, int* idx, float* wts) {
   const int lane = threadIdx.x & 31;
@@ -87,7 +88,7 @@ __device__ __forceinline__ void warp_topk(const float* logits, int E, int k, int
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    const uint32_t u = __float_as_uint(val[i]);
+    const uint32_t u = __float_as_uint(val[i] == 0.f ? 0.f : val[i]);   // -0 ties +0
     uint32_t kk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     if (val[i] != val[i]) kk = 1u;
     key[i] = e < E ? max(kk, 1u) : 0u;
@@ -178,6 +179,7 @@ struct B1Args {
   float* h_out;            // [k + S][f] fp32: w_slot * ts_down * silu(g) * u
   int* status;
   int f, E, k, S, rmax;
+  int dbg;                 // debug flags (MOE_DEBUG_FORCE_TIMEOUT)
 };
 
 struct Seg {
@@ -411,6 +413,8 @@ __global__ void __launch_bounds__(kB1Threads, 1) experts_b1_kernel(B1Args a) {
     }
   }
   if (!ok) latch_status(a.status, MOE_ERR_TIMEOUT);
+  // after every wait completed, the debug flag reports a timeout anyway
+  if (threadIdx.x == 0 && (a.dbg & MOE_DEBUG_FORCE_TIMEOUT)) latch_status(a.status, MOE_ERR_TIMEOUT);
 }
 
 // ---------------------------------------------------------------------------
@@ -437,6 +441,7 @@ struct DnArgs {
   const uint8_t* dn_scales;       // [n_all][d][f/16]
   int* status;
   int d, f, E, k, S, residual;
+  int dbg;                        // debug flags (MOE_DEBUG_FORCE_TIMEOUT)
 };
 
 // shared-memory plan of down_b1 for NS slots (byte offsets)
@@ -521,6 +526,7 @@ __global__ void __launch_bounds__(kDThreads) down_b1_kernel(DnArgs a) {
   __syncthreads();
   const bool ok = wait_parity(&bar, 0);
   if (!ok) latch_status(a.status, MOE_ERR_TIMEOUT);
+  if (threadIdx.x == 0 && (a.dbg & MOE_DEBUG_FORCE_TIMEOUT)) latch_status(a.status, MOE_ERR_TIMEOUT);
 
   // MMA lane roles: gq = lane / 4 is the A row (and B column), c = lane % 4
   // the quad position; B columns 0 (hi) and 1 (lo) come from lanes 0..7.
@@ -661,6 +667,7 @@ cudaError_t launch_experts_b1(const moe_ctx* c, const __nv_bfloat16* x, __nv_bfl
   a.k = c->cfg.top_k;
   a.S = c->cfg.n_shared;
   a.rmax = c->b1_rmax;
+  a.dbg = c->debug_flags;
   cudaError_t e = c->cfg.d_model == 2048
                       ? launch_pdl(experts_b1_kernel<2048>, dim3(c->b1_grid), dim3(kB1Threads), c->b1_smem, s, a)
                       : launch_pdl(experts_b1_kernel<4096>, dim3(c->b1_grid), dim3(kB1Threads), c->b1_smem, s, a);
@@ -679,6 +686,7 @@ cudaError_t launch_experts_b1(const moe_ctx* c, const __nv_bfloat16* x, __nv_bfl
   d.k = c->cfg.top_k;
   d.S = c->cfg.n_shared;
   d.residual = residual;
+  d.dbg = c->debug_flags;
   return launch_pdl(down_b1_kernel<512>, dim3(d.d / kRD), dim3(kDThreads), down_smem(c->cfg), s, d);
 }
 

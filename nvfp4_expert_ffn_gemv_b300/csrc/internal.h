@@ -73,10 +73,23 @@ struct moe_ctx {
 
   cudaEvent_t prof_start = nullptr;
   cudaEvent_t prof_stop = nullptr;
+
+  // debugging (moe_set_debug): flags, logits of the last routing
+  int debug_flags = 0;
+  float* dbg_logits = nullptr;   // [max_tokens][E]
+  int last_route_T = 0;          // tokens of the last routing
+  int last_route_b1 = 0;         // 1 when it was the batch-1 path (logits in `logits`)
+  int last_route_kept = 0;       // 1 when its logits were kept
 };
 
 namespace nvmoe {
 
+// Where the top-k kernels store the logits they ranked: the context's debug
+// buffer while MOE_DEBUG_KEEP_LOGITS is set, otherwise nowhere.
+inline float* debug_logits(const moe_ctx* c) {
+  return (c->debug_flags & MOE_DEBUG_KEEP_LOGITS) ? c->dbg_logits : nullptr;
+}
+cudaError_t launch_wait_selftest(int* status, uint32_t spin_limit, cudaStream_t s);
 cudaError_t launch_router(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
 cudaError_t launch_bucket(const moe_ctx* c, int T, cudaStream_t s);
 int bucket_kernel_count(int T);   // kernels launch_bucket() issues for T tokens
@@ -89,7 +102,7 @@ cudaError_t launch_quantize_nvfp4(const float* w, int n, int rows, int K, uint8_
                                   uint8_t* scales, float* ts, cudaStream_t s);
 int router_chunks(int d, int T);
 cudaError_t launch_router_topk(const float* part, const float* bias, int has_bias, int T, int E, int K, int nkc,
-                               int32_t* idx, float* w, int* status, cudaStream_t s);
+                               int32_t* idx, float* w, int* status, float* logits_out, cudaStream_t s);
 constexpr int kRTcChunks = 4;   // K chunks of the tensor-core router
 constexpr int kRTcMinTokens = 256;
 int router_tc_padded_experts(const moe_config& c);

@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include "internal.h"
@@ -76,6 +77,7 @@ size_t carve(moe_ctx* x, uint8_t* base) {
   x->r.chunk_cnt = cv.take<int32_t>(base, ((T + 31) / 32) * E);
   x->r.group_cnt = cv.take<int32_t>(base, ((T + 255) / 256) * E);
   x->r.rank = cv.take<int32_t>(base, T * k);
+  x->dbg_logits = cv.take<float>(base, T * E);
   x->h = cv.take<float>(base, P * f);
   x->yexp = cv.take<float>(base, P * d);
   x->status = cv.take<int>(base, 1);
@@ -130,6 +132,17 @@ cudaError_t copy_gu_rows(uint8_t* dst_base, const void* src, size_t row_bytes, i
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// Test hook (moe_debug_fail_alloc): the n-th device allocation from now on fails.
+std::atomic<int> g_fail_alloc_countdown{0};
+
+cudaError_t device_alloc(uint8_t** p, size_t bytes) {
+  int n = g_fail_alloc_countdown.load();
+  while (n > 0 && !g_fail_alloc_countdown.compare_exchange_weak(n, n - 1)) {
+  }
+  if (n == 1) return cudaErrorMemoryAllocation;   // this call was the n-th: fail without allocating
+  return cudaMalloc(p, bytes);
 }
 
 void ensure_device(int dev) {
@@ -187,17 +200,13 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
   x->device = device;
   x->n_all = c.n_experts + c.n_shared;
   cudaDeviceGetAttribute(&x->sm_count, cudaDevAttrMultiProcessorCount, device);
-  if (b1_supported(c)) {
-    const char* env = getenv("NVFP4_MOE_B1_CTAS_PER_SM");
-    const int per_sm = env ? atoi(env) : 1;
-    x->b1_enabled = b1_plan(c, x->sm_count, per_sm > 0 ? per_sm : 1, &x->b1_grid, &x->b1_rmax, &x->b1_nbmax,
-                            &x->b1_smem);
-  }
+  if (b1_supported(c))
+    x->b1_enabled = b1_plan(c, x->sm_count, 1, &x->b1_grid, &x->b1_rmax, &x->b1_nbmax, &x->b1_smem);
   x->pf_enabled = prefill_supported(c);
   x->mma_enabled = mma_decode_supported(c);
   x->rt_enabled = x->pf_enabled && router_tc_supported(c) && c.max_tokens >= kRTcMinTokens;
   x->arena_bytes = carve(x, nullptr);
-  if (cudaMalloc(&x->arena, x->arena_bytes) != cudaSuccess) {
+  if (device_alloc(&x->arena, x->arena_bytes) != cudaSuccess) {
     cudaGetLastError();
     delete x;
     return MOE_ERR_OOM;
@@ -292,6 +301,13 @@ moe_status moe_destroy(moe_ctx* x) {
   return cuda_status(e);
 }
 
+// Remember what the last routing of the context was (for moe_debug_logits).
+static void note_routing(moe_ctx* x, int T, int b1) {
+  x->last_route_T = T;
+  x->last_route_b1 = b1;
+  x->last_route_kept = b1 || (x->debug_flags & MOE_DEBUG_KEEP_LOGITS) != 0;
+}
+
 static moe_status check_fwd(moe_ctx* x, const void* in, int T, const void* out) {
   if (!x) return MOE_ERR_INVALID_ARG;
   if (T < 0 || T > x->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
@@ -309,6 +325,7 @@ moe_status moe_route(moe_ctx* x, const void* x_bf16, int T, int32_t* idx, float*
   const auto* xb = static_cast<const __nv_bfloat16*>(x_bf16);
   CK(launch_router(x, xb, T, s));
   CK(launch_bucket(x, T, s));
+  note_routing(x, T, 0);
   const size_t tk = (size_t)T * x->cfg.top_k;
   if (idx) CK(cudaMemcpyAsync(idx, x->r.idx, tk * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
   if (w) CK(cudaMemcpyAsync(w, x->r.w, tk * sizeof(float), cudaMemcpyDeviceToDevice, s));
@@ -330,7 +347,7 @@ static bool device_reachable(const void* p) {
 
 moe_status moe_route_noalloc(const void* x_bf16, int T, const float* router, const float* router_bias,
                              int d_model, int n_experts, int top_k, int32_t* idx, float* w, cudaStream_t s) {
-  if (T < 0 || d_model < 256 || d_model > 8192 || d_model % 256 != 0 || n_experts < 1 || n_experts > 256 ||
+  if (T < 0 || d_model < 256 || d_model > 4096 || d_model % 256 != 0 || n_experts < 1 || n_experts > 256 ||
       top_k < 1 || top_k > 8 || top_k > n_experts)
     return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
@@ -358,11 +375,13 @@ moe_status moe_forward_decode(moe_ctx* x, const void* x_bf16, int T, void* y_bf1
     if (x->prof_start) CK(cudaEventRecordWithFlags(x->prof_start, s, cudaEventRecordExternal));
     CK(launch_router_b1(x, xb, s));
     CK(launch_experts_b1(x, xb, static_cast<__nv_bfloat16*>(y_bf16), residual, s));
+    note_routing(x, 1, 1);
     if (x->prof_stop) CK(cudaEventRecordWithFlags(x->prof_stop, s, cudaEventRecordExternal));
     return MOE_OK;
   }
   CK(launch_router(x, xb, T, s));
   CK(launch_bucket(x, T, s));
+  note_routing(x, T, 0);
   if (x->prof_start) CK(cudaEventRecordWithFlags(x->prof_start, s, cudaEventRecordExternal));
   if (x->mma_enabled) {
     CK(launch_mma_decode(x, xb, T, s));
@@ -391,6 +410,7 @@ moe_status moe_forward_prefill(moe_ctx* x, const void* x_bf16, int T, void* y_bf
     CK(launch_router(x, xb, T, s));
   }
   CK(launch_bucket(x, T, s));
+  note_routing(x, T, 0);
   if (x->prof_start) CK(cudaEventRecordWithFlags(x->prof_start, s, cudaEventRecordExternal));
   CK(launch_prefill_experts(x, xb, T, s));
   if (x->prof_stop) CK(cudaEventRecordWithFlags(x->prof_stop, s, cudaEventRecordExternal));
@@ -432,6 +452,33 @@ moe_status moe_set_profile_events(moe_ctx* x, cudaEvent_t start, cudaEvent_t sto
   if (!x) return MOE_ERR_INVALID_ARG;
   x->prof_start = start;
   x->prof_stop = stop;
+  return MOE_OK;
+}
+
+moe_status moe_set_debug(moe_ctx* x, int flags) {
+  if (!x || (flags & ~(MOE_DEBUG_KEEP_LOGITS | MOE_DEBUG_FORCE_TIMEOUT))) return MOE_ERR_INVALID_ARG;
+  x->debug_flags = flags;
+  return MOE_OK;
+}
+
+moe_status moe_debug_logits(moe_ctx* x, int T, float* logits, cudaStream_t s) {
+  if (!x || !logits || T <= 0 || T != x->last_route_T || !x->last_route_kept) return MOE_ERR_INVALID_ARG;
+  ensure_device(x->device);
+  const float* src = x->last_route_b1 ? x->logits : x->dbg_logits;
+  CK(cudaMemcpyAsync(logits, src, (size_t)T * x->cfg.n_experts * sizeof(float), cudaMemcpyDeviceToDevice, s));
+  return MOE_OK;
+}
+
+moe_status moe_debug_wait_selftest(moe_ctx* x, int spin_limit, cudaStream_t s) {
+  if (!x || spin_limit < 1) return MOE_ERR_INVALID_ARG;
+  ensure_device(x->device);
+  CK(launch_wait_selftest(x->status, (uint32_t)spin_limit, s));
+  return MOE_OK;
+}
+
+moe_status moe_debug_fail_alloc(int n) {
+  if (n < 0) return MOE_ERR_INVALID_ARG;
+  g_fail_alloc_countdown.store(n);
   return MOE_OK;
 }
 

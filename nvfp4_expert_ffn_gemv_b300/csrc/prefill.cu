@@ -176,6 +176,7 @@ struct GemmArgs {
   float* yexp;            // [positions][d]
   int d;
   int* status;
+  int dbg;                // debug flags (MOE_DEBUG_FORCE_TIMEOUT)
 };
 
 // Active-expert tables copied to shared memory once per CTA, so that mapping a
@@ -419,6 +420,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // every wait has completed or given up; the debug flag reports a timeout anyway
+  if (threadIdx.x == 0 && (g.dbg & MOE_DEBUG_FORCE_TIMEOUT)) latch_status(g.status, MOE_ERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -511,6 +514,7 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   g.r = c->r;
   g.tsc = c->tsc;
   g.status = c->status;
+  g.dbg = c->debug_flags;
   g.f = f;
   g.d = d;
   // gate/up + SwiGLU + h quantisation

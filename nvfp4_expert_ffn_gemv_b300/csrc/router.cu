@@ -181,18 +181,26 @@ __global__ void __launch_bounds__(kStagedThreads, 1) router_partial_staged_kerne
 }
 
 // k rounds of warp argmax over the (up to) 256 logits v[i] of expert lane + 32 i
-// (larger value first, ties to the lower expert, NaN below every number);
+// (larger value first, equal values -- +0 and -0 included -- to the lower
+// expert, NaN below every number); logits_out (debug, or NULL) receives the
+// values ranked;
 // lanes j < K write idx and the renormalised softmax weight of token t's
 // choice j.  Each value maps to an order-preserving unsigned key, so a round
 // is a lane-local 8-way argmax, one warp max of the keys and one warp min of
 // the expert index among the lanes that hold the maximum.
 __device__ __forceinline__ void warp_select(const float (&v)[8], int E, int K, int t, int32_t* __restrict__ idx,
-                                            float* __restrict__ wout, int* status) {
+                                            float* __restrict__ wout, int* status, float* __restrict__ logits_out) {
   const int lane = threadIdx.x & 31;
+  if (logits_out) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (lane + 32 * i < E) logits_out[(size_t)t * E + lane + 32 * i] = v[i];
+  }
   uint32_t key[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint32_t u = __float_as_uint(v[i]);
+    // -0 and +0 are equal logits: both get the key of +0
+    const uint32_t u = __float_as_uint(v[i] == 0.f ? 0.f : v[i]);
     uint32_t kk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     if (v[i] != v[i]) kk = 1u;
     key[i] = lane + 32 * i < E ? max(kk, 1u) : 0u;   // 0: no expert
@@ -241,7 +249,7 @@ __device__ __forceinline__ void warp_select(const float (&v)[8], int E, int K, i
 // Many K chunks: one CTA per token; thread e sums its nkc partials in order.
 __global__ void __launch_bounds__(256) router_topk_kernel(
     const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
-    int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status) {
+    int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status, float* logits_out) {
   __shared__ float lg[256];
   const int t = blockIdx.x;
   const int e = threadIdx.x;
@@ -268,13 +276,13 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
     const int ee = threadIdx.x + 32 * i;
     v[i] = ee < E ? lg[ee] : 0.f;
   }
-  warp_select(v, E, K, t, idx, wout, status);
+  warp_select(v, E, K, t, idx, wout, status, logits_out);
 }
 
 // Few K chunks (nkc <= 4): one warp per token, the same sums in the same order.
 __global__ void __launch_bounds__(256) router_topk_warp_kernel(
     const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
-    int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status) {
+    int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status, float* logits_out) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -297,7 +305,7 @@ __global__ void __launch_bounds__(256) router_topk_warp_kernel(
     if (ee < E && has_bias) s += bias[ee];
     v[i] = s;
   }
-  warp_select(v, E, K, t, idx, wout, status);
+  warp_select(v, E, K, t, idx, wout, status, logits_out);
 }
 
 int router_tile(int T) { return T >= 256 ? 32 : 8; }
@@ -305,11 +313,12 @@ int router_tile(int T) { return T >= 256 ? 32 : 8; }
 }  // namespace
 
 cudaError_t launch_router_topk(const float* part, const float* bias, int has_bias, int T, int E, int K, int nkc,
-                               int32_t* idx, float* w, int* status, cudaStream_t s) {
+                               int32_t* idx, float* w, int* status, float* logits_out, cudaStream_t s) {
   if (nkc <= 4)
-    router_topk_warp_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status);
+    router_topk_warp_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status,
+                                                         logits_out);
   else
-    router_topk_kernel<<<T, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status);
+    router_topk_kernel<<<T, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status, logits_out);
   return cudaGetLastError();
 }
 
@@ -317,7 +326,7 @@ namespace {
 
 cudaError_t launch_router_kernels(const __nv_bfloat16* x, int T, const float* wr, const float* bias,
                                   int has_bias, int d, int E, int K, float* part, int32_t* idx, float* w,
-                                  int* status, cudaStream_t s) {
+                                  int* status, float* logits_out, cudaStream_t s) {
   const int nkc = router_chunks(d, T);
   const int tt = router_tile(T);
   const dim3 g1(nkc, (T + tt - 1) / tt);
@@ -330,7 +339,7 @@ cudaError_t launch_router_kernels(const __nv_bfloat16* x, int T, const float* wr
     router_partial_kernel<8><<<g1, 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  return launch_router_topk(part, bias, has_bias, T, E, K, nkc, idx, w, status, s);
+  return launch_router_topk(part, bias, has_bias, T, E, K, nkc, idx, w, status, logits_out, s);
 }
 
 // Scratch of the allocation-free router entry point: the split-K partial
@@ -369,7 +378,7 @@ int router_chunks(int d, int T) {
 
 cudaError_t launch_router(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s) {
   return launch_router_kernels(x, T, c->router, c->bias, c->has_bias, c->cfg.d_model, c->cfg.n_experts,
-                               c->cfg.top_k, c->router_partial, c->r.idx, c->r.w, c->status, s);
+                               c->cfg.top_k, c->router_partial, c->r.idx, c->r.w, c->status, debug_logits(c), s);
 }
 
 size_t router_static_capacity() { return kStaticPartials; }
@@ -387,7 +396,7 @@ cudaError_t launch_router_static(const __nv_bfloat16* x, int T, const float* wr,
     if ((err = prepare_router_kernels()) != cudaSuccess) return err;
     if (dev < kMaxCachedDevices) g_static_partials_addr[dev].store(part, std::memory_order_release);
   }
-  return launch_router_kernels(x, T, wr, bias, bias != nullptr, d, E, K, part, idx, w, nullptr, s);
+  return launch_router_kernels(x, T, wr, bias, bias != nullptr, d, E, K, part, idx, w, nullptr, nullptr, s);
 }
 
 }  // namespace nvmoe

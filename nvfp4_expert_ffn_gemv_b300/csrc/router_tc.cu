@@ -45,6 +45,7 @@ struct RouterTcArgs {
   float* part;      // [nkc][T][E]
   int T, E, Ep, kc_len;
   int* status;
+  int dbg;          // debug flags (MOE_DEBUG_FORCE_TIMEOUT)
 };
 
 __global__ void __launch_bounds__(kRThreads, 1)
@@ -153,6 +154,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // every wait has completed or given up; the debug flag reports a timeout anyway
+  if (threadIdx.x == 0 && (g.dbg & MOE_DEBUG_FORCE_TIMEOUT)) latch_status(g.status, MOE_ERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, tcols);
@@ -234,11 +237,12 @@ cudaError_t launch_router_tc(const moe_ctx* c, const __nv_bfloat16* x, int T, cu
   g.Ep = Ep;
   g.kc_len = d / kRTcChunks;
   g.status = c->status;
+  g.dbg = c->debug_flags;
   router_tc_kernel<<<dim3((T + kRM - 1) / kRM, kRTcChunks), kRThreads, kRSmem, s>>>(tmx, c->rt_tmw, g);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_router_topk(c->rt_part, c->bias, c->has_bias, T, E, c->cfg.top_k, kRTcChunks, c->r.idx, c->r.w,
-                            c->status, s);
+                            c->status, debug_logits(c), s);
 }
 
 }  // namespace nvmoe

@@ -47,12 +47,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+// Bounded wait for the phase with the given parity to complete: false after
+// `limit` unsuccessful polls.
+__device__ __forceinline__ bool wait_parity_n(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
   }
   return false;
+}
+
+__device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity) {
+  return wait_parity_n(bar, parity, kSpinLimit);
 }
 
 // ---------------------------------------------------------------------------

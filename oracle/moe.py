@@ -103,13 +103,21 @@ def router_logits(x: np.ndarray, router: np.ndarray, bias=None) -> np.ndarray:
     return l.astype(F32)
 
 
+def _rank_key(value: float, e: int):
+    """Sort key of expert e's logit: larger values first, equal values (+0 and -0
+    included) to the lower index, NaN after every number."""
+    if value != value:
+        return (1, 0.0, e)
+    return (0, -value, e)
+
+
 def top_k(logits: np.ndarray, k: int) -> np.ndarray:
-    """Indices of the k largest logits per row, descending; ties to the lower index."""
+    """Indices of the k largest logits per row, descending; ties to the lower index; NaN last."""
     logits = np.asarray(logits, F32)
     T, E = logits.shape
     out = np.empty((T, k), np.int32)
     for t in range(T):
-        order = sorted(range(E), key=lambda e: (-float(logits[t, e]), e))
+        order = sorted(range(E), key=lambda e: _rank_key(float(logits[t, e]), e))
         out[t] = order[:k]
     return out
 

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import synth
-from oracle import moe as omoe
+from oracle import cpp
 from tests import harness
 
 pytestmark = pytest.mark.gpu
@@ -42,21 +42,25 @@ def test_stack_chain_layerwise(lib):
                                   for _ in range(N_LAYERS)]
             idx = torch.empty((N_LAYERS, 1, k), dtype=torch.int32, device="cuda")
             w = torch.empty((N_LAYERS, 1, k), dtype=torch.float32, device="cuda")
+            logits = torch.empty((N_LAYERS, 1, s.n_experts), dtype=torch.float32, device="cuda")
             for l, layer in enumerate(layers):
                 lib.moe_forward_decode(layer.ctx, bufs[l], 1, bufs[l + 1], 1)
                 lib.moe_debug_routing(layer.ctx, 1, idx[l], w[l])   # stream-ordered after this layer
+                lib.moe_debug_logits(layer.ctx, 1, logits[l])
             torch.cuda.synchronize()
             for layer in layers:
                 assert lib.moe_get_device_status(layer.ctx) == 0
-            idx_h = idx.cpu().numpy()
+            idx_h, lg_h = idx.cpu().numpy(), logits.cpu().numpy()
             for l, layer in enumerate(layers):
-                x_l = bufs[l].float().cpu().double().numpy()      # the exact bf16 input of layer l
+                x_l = bufs[l].float().cpu().numpy()              # the exact bf16 input of layer l
                 used = np.concatenate([idx_h[l].ravel(), np.arange(s.n_experts, s.n_all)])
-                lw = layer.oracle_weights(used)
-                ref = omoe.moe_layer(lw, x_l, k, s.n_shared)
-                if harness.check_routing(idx_h[l], ref):
-                    ref = omoe.moe_layer(lw, x_l, k, s.n_shared, force_idx=idx_h[l])
-                harness.assert_close(bufs[l + 1], omoe.residual(x_l, ref.y), f"token {t} layer {l}")
+                L = layer.oracle_weights(used)
+                ref = cpp.moe_layer(L, x_l)
+                bound = harness.logit_error_bound(x_l, layer.router.cpu().numpy())
+                if harness.check_routing(idx_h[l], ref, lg_h[l], bound):
+                    L = layer.oracle_weights(np.concatenate([used, ref.idx.ravel()]))
+                    ref = cpp.moe_layer(L, x_l, force_idx=idx_h[l])
+                harness.assert_close(bufs[l + 1], cpp.residual(x_l, ref.y), f"token {t} layer {l}")
     finally:
         for layer in layers:
             lib.moe_destroy(layer.ctx)

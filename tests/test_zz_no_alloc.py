@@ -40,9 +40,13 @@ def _route_static(lib, layer, xb, T):
     return idx, w
 
 
-@pytest.mark.parametrize("shape_name,T_list", [("tiny", [4, 1, 37]), ("flint", [1, 64, 4096, 3])])
+WIDE = synth.MoEShape(d_model=4096, n_experts=64, top_k=4, d_ff=128, n_shared=1)
+
+
+@pytest.mark.parametrize("shape_name,T_list", [("tiny", [4, 1, 37]), ("flint", [1, 64, 4096, 3]),
+                                               ("wide", [1, 16, 300])])
 def test_noalloc_matches_route(lib, shape_name, T_list):
-    shape = synth.TINY if shape_name == "tiny" else synth.FLINT
+    shape = {"tiny": synth.TINY, "flint": synth.FLINT, "wide": WIDE}[shape_name]
     bias = synth.zipf_bias(shape, seed=77) if shape_name == "flint" else None
     layer = harness.make_layer(lib, shape, seed=5, router_seed=6, fmt=0, max_tokens=max(T_list), bias=bias)
     try:
@@ -71,9 +75,10 @@ def test_noalloc_rejects_what_does_not_fit(lib):
     with pytest.raises(lib.MoEError) as e:
         lib.moe_route_noalloc(x, 4097, router, None, s.d_model, s.n_experts, s.top_k, idx, w)
     assert lib.STATUS_NAMES[e.value.status] == "MOE_ERR_UNSUPPORTED"
-    with pytest.raises(lib.MoEError) as e:
-        lib.moe_route_noalloc(x, 4, router, None, 300, s.n_experts, s.top_k, idx, w)
-    assert lib.STATUS_NAMES[e.value.status] == "MOE_ERR_INVALID_ARG"
+    for bad_d in (300, 8192):
+        with pytest.raises(lib.MoEError) as e:
+            lib.moe_route_noalloc(x, 4, router, None, bad_d, s.n_experts, s.top_k, idx, w)
+        assert lib.STATUS_NAMES[e.value.status] == "MOE_ERR_INVALID_ARG"
     with pytest.raises(lib.MoEError) as e:
         lib.moe_route_noalloc(x, 4, router, None, s.d_model, s.n_experts, s.top_k, None, w)
     assert lib.STATUS_NAMES[e.value.status] == "MOE_ERR_INVALID_ARG"
