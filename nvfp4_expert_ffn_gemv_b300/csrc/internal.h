@@ -90,6 +90,8 @@ inline float* debug_logits(const moe_ctx* c) {
   return (c->debug_flags & MOE_DEBUG_KEEP_LOGITS) ? c->dbg_logits : nullptr;
 }
 cudaError_t launch_wait_selftest(int* status, uint32_t spin_limit, cudaStream_t s);
+// Every device allocation of the library goes through here (moe_debug_fail_alloc can fail it).
+cudaError_t device_alloc(void** p, size_t bytes);
 cudaError_t launch_router(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
 cudaError_t launch_bucket(const moe_ctx* c, int T, cudaStream_t s);
 int bucket_kernel_count(int T);   // kernels launch_bucket() issues for T tokens

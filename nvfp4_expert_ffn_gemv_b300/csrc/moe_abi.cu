@@ -134,10 +134,19 @@ cudaError_t copy_gu_rows(uint8_t* dst_base, const void* src, size_t row_bytes, i
   return cudaSuccess;
 }
 
-// Test hook (moe_debug_fail_alloc): the n-th device allocation from now on fails.
-std::atomic<int> g_fail_alloc_countdown{0};
+void ensure_device(int dev) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != dev) cudaSetDevice(dev);
+}
 
-cudaError_t device_alloc(uint8_t** p, size_t bytes) {
+}  // namespace
+
+namespace nvmoe {
+
+// Test hook (moe_debug_fail_alloc): the n-th device allocation from now on fails.
+static std::atomic<int> g_fail_alloc_countdown{0};
+
+cudaError_t device_alloc(void** p, size_t bytes) {
   int n = g_fail_alloc_countdown.load();
   while (n > 0 && !g_fail_alloc_countdown.compare_exchange_weak(n, n - 1)) {
   }
@@ -145,12 +154,7 @@ cudaError_t device_alloc(uint8_t** p, size_t bytes) {
   return cudaMalloc(p, bytes);
 }
 
-void ensure_device(int dev) {
-  int cur = -1;
-  if (cudaGetDevice(&cur) != cudaSuccess || cur != dev) cudaSetDevice(dev);
-}
-
-}  // namespace
+}  // namespace nvmoe
 
 extern "C" {
 
@@ -206,7 +210,7 @@ moe_status moe_init(const moe_config* cfg, const moe_weights* wts, int device, m
   x->mma_enabled = mma_decode_supported(c);
   x->rt_enabled = x->pf_enabled && router_tc_supported(c) && c.max_tokens >= kRTcMinTokens;
   x->arena_bytes = carve(x, nullptr);
-  if (device_alloc(&x->arena, x->arena_bytes) != cudaSuccess) {
+  if (device_alloc(reinterpret_cast<void**>(&x->arena), x->arena_bytes) != cudaSuccess) {
     cudaGetLastError();
     delete x;
     return MOE_ERR_OOM;

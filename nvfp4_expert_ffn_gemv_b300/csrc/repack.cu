@@ -71,7 +71,7 @@ cudaError_t repack_b1_layouts(moe_ctx* c) {
   if (e != cudaSuccess) return e;
   uint8_t* sperm = nullptr;
   const size_t gu_rows = (size_t)n * 2 * f;
-  if ((e = cudaMalloc(&sperm, gu_rows * (d / 16))) != cudaSuccess) return e;
+  if ((e = device_alloc(reinterpret_cast<void**>(&sperm), gu_rows * (d / 16))) != cudaSuccess) return e;
   const size_t tot = gu_rows * (d / 16);
   gu_scale_perm_kernel<<<(unsigned)((tot + 255) / 256), 256>>>(c->gu_scales, sperm, gu_rows, d);
   assemble_rows_kernel<<<dim3(f, n), 128>>>(c->gu_codes, sperm, c->b1_rows, d, f);

@@ -11,9 +11,11 @@
   completed (no copy or MMA is left in flight); the status is reported once,
   and the output is the same as without the flag.  Batched decode (T >= 2)
   has no device-side waits.
-* Allocation failure: moe_debug_fail_alloc makes moe_init's arena allocation
-  fail; moe_init returns MOE_ERR_OOM, leaves device memory as it found it,
-  and the next moe_init succeeds.
+* Allocation failure: moe_debug_fail_alloc makes the n-th device allocation
+  of the library fail -- the arena of moe_init, or (n = 2 on a batch-1
+  layer) the temporary buffer of the weight repacking, after the arena has
+  been filled; moe_init returns MOE_ERR_OOM, leaves device memory as it found
+  it, and the next moe_init succeeds.
 """
 import pytest
 import torch
@@ -119,5 +121,26 @@ def test_allocation_failure_is_reported_and_leaks_nothing(lib):
         torch.cuda.synchronize()
         assert abs(torch.cuda.mem_get_info()[0] - free0) <= (2 << 20)   # the arena came back
         lib.moe_destroy(lib.moe_init(base.cfg, base.weights))   # allocation works again
+    finally:
+        lib.moe_destroy(base.ctx)
+
+
+def test_allocation_failure_after_the_arena_frees_it(lib):
+    s = synth.FLINT
+    base = harness.make_layer(lib, s, seed=synth.layer_seed(5), router_seed=synth.router_seed(5), fmt=0,
+                              max_tokens=1)
+    try:
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
+        lib.moe_debug_fail_alloc(2)      # 1: the arena (~0.5 GB), 2: the repacking buffer
+        try:
+            with pytest.raises(lib.MoEError) as e:
+                lib.moe_init(base.cfg, base.weights)
+            assert lib.STATUS_NAMES[e.value.status] == "MOE_ERR_OOM"
+        finally:
+            lib.moe_debug_fail_alloc(0)
+        torch.cuda.synchronize()
+        assert abs(torch.cuda.mem_get_info()[0] - free0) <= (2 << 20)
+        lib.moe_destroy(lib.moe_init(base.cfg, base.weights))
     finally:
         lib.moe_destroy(base.ctx)
