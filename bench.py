@@ -1,7 +1,8 @@
 """Benchmark of the NVFP4 sparse-MoE FFN layer on one B300 (or N independent replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W]
-                    [--workload decode_b1|decode_b64|stack|prefill] [--impl ours|reference]
+                    [--workload decode_b1|decode_b64|stack|prefill|prefill_32k|lm_head|dense_ffn]
+                    [--impl ours|reference]
                     [--no-cpu-baseline]
 
 Workloads (Flint-shaped layer: d_model 2048, 256 routed experts top-6 + 1
@@ -18,6 +19,10 @@ shared, d_ff 512, NVFP4 weights quantised from N(0, 0.02), fp32 router 2048x256)
              through all 47 layers.
   prefill    4096 tokens through one layer per step with the block-scaled FP4
              tensor-core GEMMs; 16 layer copies.
+  lm_head    one token through the 4-bit output layer (151,936 x 2048 NVFP4,
+             two rotating copies, 350 MB): fp32 logits.
+  dense_ffn  one token through a dense 2048 x 18,432 NVFP4 SwiGLU layer (four
+             rotating copies, 255 MB), residual added.
 
 A step is one whole pass of the path (router, top-6, bucketing, experts,
 combine) over one batch; steps are serialised as in real decode.  A chunk of
@@ -61,7 +66,12 @@ WORKLOADS = {
                     metric="MoE prefill tok/s (4096 tokens, one Flint-shaped NVFP4 MoE layer)"),
     "prefill_32k": dict(T=32768, layers=4, steps=8, chunk=2,
                         metric="MoE prefill tok/s (32768 tokens, one Flint-shaped NVFP4 MoE layer)"),
+    "lm_head": dict(T=1, layers=2, steps=2000, chunk=200,
+                    metric="lm_head decode tok/s (batch-1, 151936 x 2048 NVFP4 output layer)"),
+    "dense_ffn": dict(T=1, layers=4, steps=4000, chunk=400,
+                      metric="dense FFN decode tok/s (batch-1, 2048 x 18432 NVFP4 SwiGLU layer)"),
 }
+DENSE_WORKLOADS = ("lm_head", "dense_ffn")
 
 
 #: CUDA sources whose kernels each workload's roofline covers (every header they include)
@@ -71,6 +81,8 @@ TRAFFIC_SOURCES = {
     "decode_b64": ("decode_mma.cu", "mma_frag.cuh", "internal.h", "common.cuh"),
     "prefill": ("prefill.cu", "sm100.cuh", "internal.h", "common.cuh"),
     "prefill_32k": ("prefill.cu", "sm100.cuh", "internal.h", "common.cuh"),
+    "lm_head": ("dense_gemv.cu", "mma_frag.cuh", "sm100.cuh", "internal.h", "common.cuh"),
+    "dense_ffn": ("dense_gemv.cu", "mma_frag.cuh", "sm100.cuh", "internal.h", "common.cuh"),
 }
 
 
@@ -446,9 +458,171 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def run_dense(args):
+    """lm_head / dense FFN at batch 1: one streaming NVFP4 GEMV pass (two for the FFN) per step."""
+    import torch
+    import nvfp4_expert_ffn_gemv_b300 as lib
+    import synth
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    wl = WORKLOADS[args.workload]
+    head = args.workload == "lm_head"
+    d, V, F = D_MODEL, synth.FLINT_VOCAB, synth.FLINT_DENSE_FF
+    T, n_copies = wl["T"], args.layers or wl["layers"]
+    K, W = args.steps or wl["steps"], args.warmup
+    chunk = min(wl["chunk"], K)
+    replays = (K + chunk - 1) // chunk
+    K = replays * chunk
+    ctxs = []
+    for i in range(n_copies):
+        if head:
+            w = synth.head_weight(V, d, synth.head_seed() + 100 * rank + i, device="cuda")
+            c, sc, ts = lib.quantize(w)
+            del w
+            ctxs.append(lib.moe_head_init(V, d, dict(codes=c, scales=sc, tensor_scale=ts), T))
+        else:
+            mats = []
+            for w in synth.dense_ffn_weights(d, F, synth.dense_seed(i) + 100 * rank, device="cuda"):
+                c, sc, ts = lib.quantize(w)
+                mats.append(dict(codes=c, scales=sc, tensor_scale=ts))
+            ctxs.append(lib.moe_ffn_init(d, F, *mats, T))
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    stream = torch.cuda.Stream()
+    n_inputs = chunk + W
+    xb, _ = synth.tokens(synth.FLINT, n_inputs * T, seed=synth.token_seed(rank), device="cuda")
+    x = xb.view(n_inputs, T, d)
+    out = (torch.empty((n_inputs, T, V), dtype=torch.float32, device="cuda") if head
+           else torch.empty_like(x))
+
+    def step(i, xi=None, oi=None):
+        c = ctxs[i % n_copies]
+        xi = x[i] if xi is None else xi
+        oi = out[i] if oi is None else oi
+        if head:
+            lib.moe_head_forward(c, xi, T, oi, stream)
+        else:
+            lib.moe_ffn_forward(c, xi, T, oi, 1, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(chunk, chunk + W):
+            step(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(chunk):
+            step(i)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(chunk)]
+    for a, b in ev:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    gp = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gp, stream=stream):
+        for i in range(chunk):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+    for c in ctxs:
+        assert lib.moe_dense_get_device_status(c) == 0
+
+    def timed(graph, n):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            graph.replay()                     # untimed: device busy while the timed replays are queued
+            a.record(stream)
+            for _ in range(n):
+                graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        return a.elapsed_time(b)
+
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms = timed(g, replays)
+    with torch.cuda.stream(stream):
+        gp.replay()
+    torch.cuda.synchronize()
+    kern_ms = sorted(a.elapsed_time(b) for a, b in ev)
+    ms = max_over_ranks(ms)
+    # end to end: pinned host token in, host result out, every step
+    xh = x[:chunk].cpu().pin_memory()
+    oh = torch.empty((chunk,) + tuple(out.shape[1:]), dtype=out.dtype).pin_memory()
+    xd = torch.empty_like(x[0])
+    od = torch.empty_like(out[0])
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ge, stream=stream):
+        for i in range(chunk):
+            xd.copy_(xh[i], non_blocking=True)
+            step(i, xd, od)
+            oh[i].copy_(od, non_blocking=True)
+    with torch.cuda.stream(stream):
+        ge.replay()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(timed(ge, replays))
+    for c in ctxs:
+        lib.moe_dense_destroy(c)
+    if rank != 0:
+        return
+    hbm_peak, _, _, peak_kind = _peaks()
+    tok = world * K * T
+    step_ms = ms / K
+    alg = V * d * 9 // 16 if head else 3 * d * F * 9 // 16
+    ach = alg / step_ms / 1e6
+    kus = {"avg": round(sum(kern_ms) / len(kern_ms) * 1e3, 3), "median": round(kern_ms[len(kern_ms) // 2] * 1e3, 3)}
+    line = {
+        "metric": wl["metric"], "value": round(tok / (ms / 1e3), 1), "unit": "tok/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(step_ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 accumulate (nvfp4 weights, bf16 activations)", "data": "synthetic",
+        "config": {"workload": args.workload, "d_model": d, ("vocab" if head else "d_ff"): V if head else F,
+                   "tokens_per_step": T, "copies": n_copies,
+                   "l2": f"{n_copies} rotating weight copies ({n_copies * alg / 1e6:.0f} MB, above the 126 MB L2)",
+                   "parallelism": "independent replicas" if world > 1 else "single GPU"},
+        "gpu_launches": K * (2 if head else 5),
+        "clocks": clk.summary(),
+        "roofline": {"kernel": "streaming NVFP4 GEMV (lm_head)" if head else
+                     "dense FFN: gate/up GEMV + SwiGLU, down GEMV, slice reduction",
+                     "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(ach / hbm_peak, 4), "peak_kind": peak_kind + " copy bandwidth",
+                     "frac_of_nominal_8tbs": round(ach / HBM_NOMINAL_GBS, 4),
+                     "algorithmic_bytes_per_launch": alg, "traffic": _traffic(args.workload),
+                     "launch_us": round(step_ms * 1e3, 3), "launch_us_isolated": kus},
+        "e2e": {"value": round(tok / (e2e_ms / 1e3), 1), "unit": "tok/s", "h2d_bytes_per_step": T * d * 2,
+                "d2h_bytes_per_step": T * (V * 4 if head else d * 2)},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle arm
 # ---------------------------------------------------------------------------
+def _dense_oracle_sample(workload: str):
+    """Oracle weights of one lm_head / dense layer and one token (quantised beforehand, untimed)."""
+    import synth
+    from oracle import cpp
+    d = D_MODEL
+    _, x = synth.tokens(synth.FLINT, 1, seed=synth.token_seed(0))
+    x = x.numpy()
+    if workload == "lm_head":
+        m = cpp.quantize(synth.head_weight(synth.FLINT_VOCAB, d, synth.head_seed()).numpy())
+        return (lambda nt: cpp.gemv(*m, x, nthreads=nt)), "one token through the 151936 x 2048 output layer"
+    mats = [cpp.quantize(w.numpy()) for w in synth.dense_ffn_weights(d, synth.FLINT_DENSE_FF, synth.dense_seed(0))]
+    return (lambda nt: cpp.dense_ffn(*mats, x, nthreads=nt)), "one token through a 2048 x 18432 dense SwiGLU layer"
+
+
 def _oracle_sample(workload: str):
     """The bounded sample the CPU oracle runs: (layer, token batches, prefill flag, what).
 
@@ -501,6 +675,22 @@ def cpu_baseline(workload: str, budget_s: float = 10.0):
     """Time the C++ oracle as it stands, on a bounded sample of the workload, on all of
     the host's cores (its std::thread pool) and on one thread."""
     cores = os.cpu_count() or 1
+    if workload in DENSE_WORKLOADS:
+        fn, what = _dense_oracle_sample(workload)
+        res = []
+        for nt, budget in ((cores, budget_s), (1, budget_s / 2)):
+            t0, done = time.perf_counter(), 0
+            while True:
+                fn(nt)
+                done += 1
+                if time.perf_counter() - t0 > budget:
+                    break
+            res.append((done, time.perf_counter() - t0))
+        (done, dt), (done1, dt1) = res
+        return {"value": round(done / dt, 4), "unit": "tok/s", "cores": cores, "kind": "oracle",
+                "single_thread_value": round(done1 / dt1, 4),
+                "sample": f"{done} x 1 token: {what} (C++ oracle, weights dequantised each call), {dt:.2f} s on "
+                          f"{cores} threads; {done1} in {dt1:.2f} s on one thread"}
     layer, x, prefill, what = _oracle_sample(workload)
     T = x.shape[1]
     done, dt = _time_oracle(layer, x, prefill, cores, budget_s)
@@ -547,6 +737,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload in DENSE_WORKLOADS:
+        run_dense(args)
     else:
         run_ours(args)
 

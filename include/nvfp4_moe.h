@@ -237,6 +237,53 @@ MOE_API moe_status moe_debug_wait_selftest(moe_ctx* ctx, int spin_limit, cudaStr
  * 0 disables.  Process-wide.  The pages have no counterpart. */
 MOE_API moe_status moe_debug_fail_alloc(int n);
 
+/* ------------------------------------------------------------------------
+ * Dense NVFP4 weights every token reads in full: the output layer and the
+ * dense FFN layers.
+ *
+ * Pages: the output layer (lm_head) ships in 4 bits because, with ~2.5B
+ * active parameters, it is a large share of the weights each token reads
+ * (OrcaRouter page, section "量子化のレシピは最も転用しやすい部分です"); 2 of
+ * the 49 layers are dense (section "このアーキテクチャはメモリ帯域幅に関する主張
+ * である").  Their sizes are not on the pages; the readings taken here (vocab
+ * 151,936, dense d_ff 18,432 at d_model 2048) follow from the pages' parameter
+ * counts, but any size within the limits below is accepted.
+ *
+ * Both run as a streaming GEMV on the tensor cores with exact operands (NVFP4
+ * weights and bf16 activations exact in f16, fp32 accumulation); up to 32
+ * tokens share one pass over the weights, larger T takes several passes.
+ * Weights are copied into a library-owned arena at init (host or device
+ * pointers, canonical NVFP4 layout as above); forward calls allocate nothing,
+ * are asynchronous on `stream`, and must not overlap on one context.
+ * ------------------------------------------------------------------------ */
+typedef struct moe_dense moe_dense; /* opaque, owned by the library */
+
+/* lm_head: w = NVFP4 [vocab][d_model] (one tensor scale).  vocab % 16 == 0,
+ * d_model a power of two in 256..4096, 1 <= max_tokens <= 4096. */
+MOE_API moe_status moe_head_init(int vocab, int d_model, const moe_matrix* w, int max_tokens, int device,
+                                 moe_dense** out);
+
+/* logits [T][vocab] fp32 = x [T][d_model] bf16 . W^T; device pointers, 16-byte aligned. */
+MOE_API moe_status moe_head_forward(moe_dense* head, const void* x_bf16, int T, float* logits,
+                                    cudaStream_t stream);
+
+/* Dense SwiGLU FFN: gate, up NVFP4 [d_ff][d_model], down [d_model][d_ff].
+ * d_model a power of two in 256..4096; d_ff a multiple of 256 (at most 65536)
+ * with a divisor K slice of at most 2304 that is a multiple of 128. */
+MOE_API moe_status moe_ffn_init(int d_model, int d_ff, const moe_matrix* gate, const moe_matrix* up,
+                                const moe_matrix* down, int max_tokens, int device, moe_dense** out);
+
+/* y [T][d_model] bf16 = W_down (silu(W_gate x) * W_up x) (+ x when residual);
+ * y may not alias x. */
+MOE_API moe_status moe_ffn_forward(moe_dense* ffn, const void* x_bf16, int T, void* y_bf16, int residual,
+                                   cudaStream_t stream);
+
+/* Synchronise and return (then clear) the dense context's device status word. */
+MOE_API moe_status moe_dense_get_device_status(moe_dense* ctx);
+
+/* Free everything the dense context owns.  NULL is accepted. */
+MOE_API moe_status moe_dense_destroy(moe_dense* ctx);
+
 /* Synchronise the context's device and return the latched device status
  * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK), then clear it. */
 MOE_API moe_status moe_get_device_status(moe_ctx* ctx);

@@ -28,7 +28,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 #: every symbol the C header declares
 EXPORTS = ("moe_init", "moe_route", "moe_route_noalloc", "moe_forward_decode", "moe_forward_prefill", "moe_quantize_nvfp4",
            "moe_debug_prefill_h", "moe_debug_routing", "moe_set_profile_events", "moe_set_debug", "moe_debug_logits",
-           "moe_debug_wait_selftest", "moe_debug_fail_alloc", "moe_get_device_status",
+           "moe_debug_wait_selftest", "moe_debug_fail_alloc", "moe_head_init", "moe_head_forward", "moe_ffn_init",
+           "moe_ffn_forward", "moe_dense_get_device_status", "moe_dense_destroy", "moe_get_device_status",
            "moe_kernels_per_forward", "moe_destroy", "moe_status_string")
 MOE_DEBUG_KEEP_LOGITS = 1
 MOE_DEBUG_FORCE_TIMEOUT = 2
@@ -77,6 +78,12 @@ def _load():
         "moe_debug_logits": (i, [vp, i, vp, vp]),
         "moe_debug_wait_selftest": (i, [vp, i, vp]),
         "moe_debug_fail_alloc": (i, [i]),
+        "moe_head_init": (i, [i, i, p(moe_matrix), i, i, p(vp)]),
+        "moe_head_forward": (i, [vp, vp, i, vp, vp]),
+        "moe_ffn_init": (i, [i, i, p(moe_matrix), p(moe_matrix), p(moe_matrix), i, i, p(vp)]),
+        "moe_ffn_forward": (i, [vp, vp, i, vp, i, vp]),
+        "moe_dense_get_device_status": (i, [vp]),
+        "moe_dense_destroy": (i, [vp]),
         "moe_get_device_status": (i, [vp]),
         "moe_kernels_per_forward": (i, [vp, i, i]),
         "moe_destroy": (i, [vp]),
@@ -197,6 +204,40 @@ def moe_debug_wait_selftest(ctx, spin_limit: int, stream=None) -> None:
 
 def moe_debug_fail_alloc(n: int) -> None:
     _check("moe_debug_fail_alloc", _lib.moe_debug_fail_alloc(int(n)))
+
+
+def moe_head_init(vocab: int, d_model: int, w: dict, max_tokens: int, device: int = 0):
+    """lm_head context from w = dict(codes=, scales=, tensor_scale=) (host or device tensors)."""
+    out = ctypes.c_void_p()
+    m = _matrix(w)
+    _check("moe_head_init", _lib.moe_head_init(int(vocab), int(d_model), ctypes.byref(m), int(max_tokens),
+                                               int(device), ctypes.byref(out)))
+    return out.value
+
+
+def moe_head_forward(ctx, x, T: int, logits, stream=None) -> None:
+    _check("moe_head_forward", _lib.moe_head_forward(ctx, _ptr(x), int(T), _ptr(logits), _stream(stream)))
+
+
+def moe_ffn_init(d_model: int, d_ff: int, gate: dict, up: dict, down: dict, max_tokens: int, device: int = 0):
+    """Dense SwiGLU FFN context from NVFP4 gate/up/down dicts (codes, scales, tensor_scale)."""
+    out = ctypes.c_void_p()
+    g, u, d = _matrix(gate), _matrix(up), _matrix(down)
+    _check("moe_ffn_init", _lib.moe_ffn_init(int(d_model), int(d_ff), ctypes.byref(g), ctypes.byref(u),
+                                             ctypes.byref(d), int(max_tokens), int(device), ctypes.byref(out)))
+    return out.value
+
+
+def moe_ffn_forward(ctx, x, T: int, y, residual: int = 0, stream=None) -> None:
+    _check("moe_ffn_forward", _lib.moe_ffn_forward(ctx, _ptr(x), int(T), _ptr(y), int(residual), _stream(stream)))
+
+
+def moe_dense_get_device_status(ctx) -> int:
+    return int(_lib.moe_dense_get_device_status(ctx))
+
+
+def moe_dense_destroy(ctx) -> None:
+    _check("moe_dense_destroy", _lib.moe_dense_destroy(ctx))
 
 
 def moe_get_device_status(ctx) -> int:

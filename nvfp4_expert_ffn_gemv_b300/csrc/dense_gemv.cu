@@ -1,0 +1,638 @@
+// Streaming NVFP4 GEMV for the weights every token reads in full: the 4-bit
+// output layer (lm_head) and the two dense SwiGLU FFN layers.
+//
+// The pages say the vendor quantised the output layer to 4 bits because, with
+// only ~2.5B active parameters, it is a large share of the weights a token
+// reads ("Recursive Flint 40B-A2.5B：まず速さを第一に考えて作られたコーディング
+// モデル", section "量子化のレシピは最も転用しやすい部分です"), and that 2 of
+// the 49 layers are dense (section "このアーキテクチャはメモリ帯域幅に関する主張
+// である").  At decode both are one pass over a large NVFP4 matrix per token
+// batch, so the kernel is built to keep HBM busy:
+//
+//   * persistent CTAs, one per SM; the matrix is cut into units of 16 rows x
+//     one K slice, unit u going to CTA u % grid;
+//   * warp 0 streams units with TMA bulk copies (codes and E4M3 scales of a
+//     unit are contiguous) into a ring of up to 8 shared-memory stages;
+//     consumer warp w owns stage w, so a stage is refilled as soon as its
+//     warp is done with it and ~150 KB per SM stay in flight;
+//   * the consumer multiplies on the tensor cores (mma.sync m16n8k16, f16 in,
+//     fp32 accumulate) with exact operands: A = E2M1 code x E4M3 block scale
+//     (at most 6 significant bits, exact in f16), B = the activations, bf16
+//     after a per-token power-of-two prescale (exact in f16), or for the down
+//     projection the fp32 hidden vector split into f16 hi + lo; every product
+//     is exact, only the fp32 sums round.  Up to 32 tokens share one pass over
+//     the weights (4 MMA column groups); larger batches take several passes.
+//
+// Epilogues: lm_head writes fp32 logits; the dense gate/up pass (tiles of 8
+// gate rows + the matching 8 up rows) applies SwiGLU in registers and writes
+// h (fp32); the dense down pass writes fp32 partial sums per K slice, which a
+// small kernel adds in a fixed order (plus the residual) into bf16 y.
+#include "internal.h"
+#include "mma_frag.cuh"
+#include "sm100.cuh"
+
+namespace nvmoe {
+
+namespace {
+
+using namespace sm100;
+using namespace frag;
+
+constexpr int kMaxStages = 8;
+constexpr int kTokPass = 32;          // tokens per pass over the weights (4 column groups of 8)
+constexpr int kStageBudget = 196608;  // shared-memory bytes for the stage ring
+
+enum GemvMode { kModeHead = 0, kModeGateUp = 1, kModeDown = 2 };
+
+struct GemvArgs {
+  const uint8_t* codes;    // unit (slice s, tile t): codes + s * slice_codes + t * 16 * KS / 2
+  const uint8_t* scales;   //                          scales + s * slice_scales + t * 16 * KS / 16
+  size_t slice_codes, slice_scales;
+  int ntiles, nslices, KS;
+  const uint8_t* b_hi;     // B operand [kTokPass][K] f16, prescaled, k-permuted per 128 chunk
+  const uint8_t* b_lo;     // down: low halves of h (same layout); otherwise null
+  int K;                   // full row length of the B operand
+  const float* unshift;    // [kTokPass] 2^-prescale of each token
+  int T;                   // tokens of this pass (<= kTokPass)
+  float ts0, ts1;          // tensor scales (head: ts0; gate/up: ts0 gate, ts1 up; down: ts0)
+  float* out;              // head [T][out_ld] logits; gate/up [T][out_ld] h; down [S][T][out_ld] partials
+  int out_ld;
+  int nstages;             // stages = consumer warps
+  int* status;
+  int dbg;
+};
+
+__device__ __forceinline__ uint2 ldg64(const uint8_t* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+
+template <int MODE, int NG>
+__device__ __forceinline__ void consume_unit(const GemvArgs& g, const uint8_t* sc, const uint8_t* ss, int slice,
+                                             int tile) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, c = lane & 3;
+  const int KS = g.KS, CB = KS / 2, SB = KS / 16;
+  float acc[NG][4];
+#pragma unroll
+  for (int q = 0; q < NG; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+  const uint8_t* row0 = sc + gq * CB + c * 16;
+  const uint8_t* row8 = row0 + 8 * CB;
+  const uint8_t* srow0 = ss + gq * SB + c * 2;
+  const uint8_t* srow8 = srow0 + 8 * SB;
+  const size_t brow = (size_t)g.K * 2;
+  const int k0 = slice * KS;     // first k of this unit in the B operand
+  for (int ch = 0; ch < KS / 128; ++ch) {
+    const uint4 wc = *reinterpret_cast<const uint4*>(row0 + ch * 64);
+    const uint4 wc8 = *reinterpret_cast<const uint4*>(row8 + ch * 64);
+    const uint32_t s2 = cvt_e4m3x2_f16x2(*reinterpret_cast<const uint16_t*>(srow0 + ch * 8));
+    const uint32_t s28 = cvt_e4m3x2_f16x2(*reinterpret_cast<const uint16_t*>(srow8 + ch * 8));
+    const size_t boff = (size_t)(k0 + ch * 128) * 2;
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+      const uint32_t sg = wd < 2 ? bcast_lo(s2) : bcast_hi(s2);
+      const uint32_t sg8 = wd < 2 ? bcast_lo(s28) : bcast_hi(s28);
+      uint32_t afp[2][4];
+      a_frag_pair(afp[0], afp[1], word_of(wc, wd), word_of(wc8, wd), sg, sg8);
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int kk = 2 * wd + h2;
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+          const size_t off = (size_t)(8 * q + gq) * brow + boff + perm_off(c, kk);
+          const uint2 b = ldg64(g.b_hi + off);
+          mma_f16(acc[q], afp[h2], b.x, b.y);
+          if (MODE == kModeDown) {
+            const uint2 bl = ldg64(g.b_lo + off);
+            mma_f16(acc[q], afp[h2], bl.x, bl.y);
+          }
+        }
+      }
+    }
+  }
+  // lanes hold rows gq (acc 0, 1) and gq + 8 (acc 2, 3) of the tile, tokens 8q + 2c, 8q + 2c + 1
+#pragma unroll
+  for (int q = 0; q < NG; ++q) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int t = 8 * q + 2 * c + j;
+      if (t >= g.T) continue;
+      const float un = g.unshift[t];
+      if (MODE == kModeHead) {
+        const int r = tile * 16 + gq;
+        g.out[(size_t)t * g.out_ld + r] = acc[q][j] * g.ts0 * un;
+        g.out[(size_t)t * g.out_ld + r + 8] = acc[q][2 + j] * g.ts0 * un;
+      } else if (MODE == kModeGateUp) {
+        const float gv = acc[q][j] * g.ts0 * un, uv = acc[q][2 + j] * g.ts1 * un;
+        g.out[(size_t)t * g.out_ld + tile * 8 + gq] = silu_f(gv) * uv;
+      } else {
+        float* dst = g.out + ((size_t)slice * g.T + t) * g.out_ld + tile * 16 + gq;
+        dst[0] = acc[q][j] * g.ts0 * un;
+        dst[8] = acc[q][2 + j] * g.ts0 * un;
+      }
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(32 * (kMaxStages + 1), 1) nvfp4_gemv_kernel(GemvArgs g) {
+  extern __shared__ __align__(128) uint8_t gsm[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NS = g.nstages;
+  const uint32_t ucodes = 16u * (uint32_t)g.KS / 2, uscales = 16u * (uint32_t)g.KS / 16;
+  const uint32_t stage_bytes = ucodes + uscales;
+  const int units = g.ntiles * g.nslices;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  bool ok = true;
+  if (warp == 0) {
+    if (lane == 0) {
+      int j = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
+        const int s = j % NS;
+        if (j >= NS && !wait_parity(&empty_bar[s], ((j / NS) - 1) & 1)) { ok = false; break; }
+        const int slice = u / g.ntiles, tile = u % g.ntiles;
+        uint8_t* dst = gsm + (size_t)s * stage_bytes;
+        mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
+        bulk_load(dst, g.codes + slice * g.slice_codes + (size_t)tile * ucodes, ucodes, &full_bar[s]);
+        bulk_load(dst + ucodes, g.scales + slice * g.slice_scales + (size_t)tile * uscales, uscales, &full_bar[s]);
+      }
+      // every copy issued here lands before the consumer that owns its stage
+      // finishes, and the CTA leaves only after all consumers (below)
+    }
+  } else if (warp - 1 < NS) {
+    const int s = warp - 1;
+    int j = s;
+    for (int u = blockIdx.x + s * gridDim.x; u < units; u += NS * gridDim.x, j += NS) {
+      if (!wait_parity(&full_bar[s], (j / NS) & 1)) { ok = false; }
+      const uint8_t* sc = gsm + (size_t)s * stage_bytes;
+      const int slice = u / g.ntiles, tile = u % g.ntiles;
+      if (ok) {
+        const int ngroups = (g.T + 7) / 8;
+        if (ngroups <= 1) consume_unit<MODE, 1>(g, sc, sc + ucodes, slice, tile);
+        else if (ngroups == 2) consume_unit<MODE, 2>(g, sc, sc + ucodes, slice, tile);
+        else consume_unit<MODE, 4>(g, sc, sc + ucodes, slice, tile);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+  }
+  if (!ok) latch_status(g.status, MOE_ERR_TIMEOUT);
+  __syncthreads();
+  if (threadIdx.x == 0 && (g.dbg & MOE_DEBUG_FORCE_TIMEOUT)) latch_status(g.status, MOE_ERR_TIMEOUT);
+}
+
+// bf16 x [T][K] -> prescaled f16 in the permuted chunk order, kTokPass rows
+// (rows T.. zero), one warp per row; unshift[t] = 2^-shift.
+__global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int K,
+                                                     uint8_t* __restrict__ out, float* __restrict__ unshift) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= kTokPass) return;
+  uint8_t* dst = out + (size_t)t * K * 2;
+  if (t >= T) {
+    for (int i = lane; i < K / 8; i += 32) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0) unshift[t] = 0.f;
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * K);
+  float m = 0.f;
+  for (int i = lane; i < K / 8; i += 32) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
+  }
+  const int shift = prescale_shift(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+  const float sc = pow2i(shift);
+  for (int i = lane; i < K / 8; i += 32) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 hh = __floats2half2_rn(__uint_as_float(w[q] << 16) * sc, __uint_as_float(w[q] & 0xFFFF0000u) * sc);
+      hv[q] = *reinterpret_cast<const uint32_t*>(&hh);
+    }
+    const int k0 = 8 * i, kp = k0 % 128, cc = kp / 32, kk = (kp % 32) / 4;
+    uint8_t* base = dst + (size_t)(k0 / 128) * 256;
+    *reinterpret_cast<uint2*>(base + perm_off(cc, kk)) = make_uint2(hv[0], hv[1]);
+    *reinterpret_cast<uint2*>(base + perm_off(cc, kk + 1)) = make_uint2(hv[2], hv[3]);
+  }
+  if (lane == 0) unshift[t] = pow2i(-shift);
+}
+
+// fp32 h [T][K] -> prescaled f16 hi + lo in the permuted chunk order (rows T.. zero).
+__global__ void __launch_bounds__(256) prep_h_kernel(const float* __restrict__ h, int T, int K, uint8_t* __restrict__ hi,
+                                                     uint8_t* __restrict__ lo, float* __restrict__ unshift) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= kTokPass) return;
+  uint8_t* dh = hi + (size_t)t * K * 2;
+  uint8_t* dl = lo + (size_t)t * K * 2;
+  if (t >= T) {
+    for (int i = lane; i < K / 8; i += 32) {
+      reinterpret_cast<uint4*>(dh)[i] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(dl)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (lane == 0) unshift[t] = 0.f;
+    return;
+  }
+  const float4* src = reinterpret_cast<const float4*>(h + (size_t)t * K);
+  float m = 0.f;
+  for (int i = lane; i < K / 4; i += 32) {
+    const float4 v = src[i];
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  const int shift = prescale_shift(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+  const float sc = pow2i(shift);
+  for (int i = lane; i < K / 4; i += 32) {
+    const float4 v = src[i];
+    uint2 vh, vl;
+    split_hi_lo(v.x * sc, v.y * sc, v.z * sc, v.w * sc, vh, vl);
+    const int k0 = 4 * i, kp = k0 % 128;
+    const size_t off = (size_t)(k0 / 128) * 256 + perm_off(kp / 32, (kp % 32) / 4);
+    *reinterpret_cast<uint2*>(dh + off) = vh;
+    *reinterpret_cast<uint2*>(dl + off) = vl;
+  }
+  if (lane == 0) unshift[t] = pow2i(-shift);
+}
+
+// y[t][r] = bf16(sum over the S K slices, in order, of partial[s][t][r] (+ x[t][r]))
+__global__ void __launch_bounds__(256) reduce_down_kernel(const float* __restrict__ part, int S, int T, int d,
+                                                          const __nv_bfloat16* __restrict__ x, int residual,
+                                                          __nv_bfloat16* __restrict__ y) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * d) return;
+  float acc = 0.f;
+  for (int s = 0; s < S; ++s) acc += part[(size_t)s * T * d + i];
+  if (residual) acc += __bfloat162float(x[i]);
+  y[i] = __float2bfloat16_rn(acc);
+}
+
+// gate/up [f][K] canonical -> tiles of 8 gate rows then the matching 8 up rows
+__global__ void interleave_gu_kernel(const uint8_t* __restrict__ gsrc, const uint8_t* __restrict__ usrc,
+                                     size_t row_bytes, int f, uint8_t* __restrict__ dst) {
+  const int r = blockIdx.x;        // destination row 0 .. 2f-1
+  const int tile = r / 16, w = r % 16;
+  const uint8_t* src = (w < 8 ? gsrc : usrc) + (size_t)(tile * 8 + (w & 7)) * row_bytes;
+  for (size_t i = threadIdx.x; i < row_bytes; i += blockDim.x) dst[(size_t)r * row_bytes + i] = src[i];
+}
+
+// W_down [d][f] canonical -> K slices [S][d][KS] (codes KS/2 or scales KS/16 bytes per row and slice)
+__global__ void slice_rows_kernel(const uint8_t* __restrict__ src, int d, size_t row_bytes, int S,
+                                  uint8_t* __restrict__ dst) {
+  const int r = blockIdx.x, s = blockIdx.y;
+  const size_t sb = row_bytes / S;
+  for (size_t i = threadIdx.x; i < sb; i += blockDim.x)
+    dst[((size_t)s * d + r) * sb + i] = src[(size_t)r * row_bytes + (size_t)s * sb + i];
+}
+
+int stages_for(int KS) {
+  const int stage = 16 * KS / 2 + 16 * KS / 16;
+  int n = kStageBudget / stage;
+  return n > kMaxStages ? kMaxStages : n;
+}
+
+size_t gemv_smem(int KS) { return (size_t)stages_for(KS) * (16 * KS / 2 + 16 * KS / 16); }
+
+template <int MODE>
+cudaError_t launch_gemv(GemvArgs g, int sm_count, cudaStream_t s) {
+  const int units = g.ntiles * g.nslices;
+  const int grid = units < sm_count ? units : sm_count;
+  g.nstages = stages_for(g.KS);
+  nvfp4_gemv_kernel<MODE><<<grid, 32 * (g.nstages + 1), gemv_smem(g.KS), s>>>(g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// host side: the dense context
+// ---------------------------------------------------------------------------
+}  // namespace nvmoe
+
+struct moe_dense {
+  int kind = 0;              // 0 lm_head, 1 dense FFN
+  int device = 0, sm_count = 0;
+  int d = 0, rows = 0, f = 0, max_tokens = 0;
+  int S = 1, KS = 0;         // K slices of the down projection
+  uint8_t* arena = nullptr;
+  uint8_t* codes = nullptr;  // head [R][d/2]; FFN gate/up tiles [2f][d/2]
+  uint8_t* scales = nullptr;
+  uint8_t* dn_codes = nullptr;   // FFN: [S][d][KS/2]
+  uint8_t* dn_scales = nullptr;  // FFN: [S][d][KS/16]
+  float ts[3] = {0.f, 0.f, 0.f};
+  uint8_t* x16 = nullptr;    // [kTokPass][d] f16
+  float* xun = nullptr;      // [kTokPass]
+  float* h = nullptr;        // FFN: [kTokPass][f]
+  uint8_t* h_hi = nullptr;   // FFN: [kTokPass][f] f16
+  uint8_t* h_lo = nullptr;
+  float* hun = nullptr;      // FFN: [kTokPass]
+  float* part = nullptr;     // FFN: [S][kTokPass][d]
+  int* status = nullptr;
+};
+
+namespace nvmoe {
+
+namespace {
+
+size_t carve_dense(moe_dense* x, uint8_t* base) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    off = (off + 255) & ~size_t(255);
+    uint8_t* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  };
+  const size_t d = x->d;
+  const size_t R = x->kind == 0 ? (size_t)x->rows : 2 * (size_t)x->f;
+  x->codes = take(R * d / 2);
+  x->scales = take(R * d / 16);
+  x->x16 = take((size_t)kTokPass * d * 2);
+  x->xun = reinterpret_cast<float*>(take(kTokPass * sizeof(float)));
+  x->status = reinterpret_cast<int*>(take(sizeof(int)));
+  if (x->kind == 1) {
+    const size_t f = x->f;
+    x->dn_codes = take(d * f / 2);
+    x->dn_scales = take(d * f / 16);
+    x->h = reinterpret_cast<float*>(take((size_t)kTokPass * f * sizeof(float)));
+    x->h_hi = take((size_t)kTokPass * f * 2);
+    x->h_lo = take((size_t)kTokPass * f * 2);
+    x->hun = reinterpret_cast<float*>(take(kTokPass * sizeof(float)));
+    x->part = reinterpret_cast<float*>(take((size_t)x->S * kTokPass * d * sizeof(float)));
+  }
+  return off;
+}
+
+bool matrix_ok(const moe_matrix* m) { return m && m->codes && m->scales && m->tensor_scale; }
+
+// K slices of the dense down projection: the largest K slice <= 2304 that is a
+// multiple of 128 and divides f (so a stage of 16 rows x K slice stays ~20 KB)
+int down_slices(int f) {
+  for (int ks = 2304; ks >= 128; ks -= 128)
+    if (f % ks == 0) return f / ks;
+  return -1;
+}
+
+moe_status alloc_dense(moe_dense* x) {
+  x->arena = nullptr;
+  const size_t bytes = carve_dense(x, nullptr);
+  if (device_alloc(reinterpret_cast<void**>(&x->arena), bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_OOM;
+  }
+  carve_dense(x, x->arena);
+  return MOE_OK;
+}
+
+cudaError_t set_gemv_smem() {
+  cudaError_t e = cudaSuccess;
+  const int big = (int)gemv_smem(4096) > (int)gemv_smem(2304) ? (int)gemv_smem(4096) : (int)gemv_smem(2304);
+  const int lim = big > kStageBudget ? big : kStageBudget;
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeHead>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  return e;
+}
+
+moe_status finish_init(moe_dense* x, cudaError_t e, moe_dense** out) {
+  if (e == cudaSuccess) e = cudaMemset(x->status, 0, sizeof(int));
+  if (e == cudaSuccess) e = set_gemv_smem();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(x->arena);
+    delete x;
+    return e == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA;
+  }
+  *out = x;
+  return MOE_OK;
+}
+
+bool is_pow2_between(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+moe_status check_dense_call(moe_dense* x, const void* in, int T, const void* out) {
+  if (!x || T < 0 || T > x->max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!in || !out || (reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(out) & 15)))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+GemvArgs base_args(const moe_dense* x, int T) {
+  GemvArgs g{};
+  g.nslices = 1;
+  g.T = T;
+  g.status = x->status;
+  g.dbg = 0;
+  return g;
+}
+
+}  // namespace
+
+}  // namespace nvmoe
+
+using namespace nvmoe;
+
+extern "C" {
+
+moe_status moe_head_init(int vocab, int d_model, const moe_matrix* w, int max_tokens, int device, moe_dense** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (vocab <= 0 || d_model <= 0 || max_tokens <= 0 || !matrix_ok(w)) return MOE_ERR_INVALID_ARG;
+  if (vocab % 16 != 0 || !is_pow2_between(d_model, 256, 4096) || max_tokens > 4096) return MOE_ERR_UNSUPPORTED;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return MOE_ERR_INVALID_ARG;
+  if (cudaSetDevice(device) != cudaSuccess) return MOE_ERR_CUDA;
+  moe_dense* x = new moe_dense();
+  x->kind = 0;
+  x->device = device;
+  x->d = d_model;
+  x->rows = vocab;
+  x->max_tokens = max_tokens;
+  cudaDeviceGetAttribute(&x->sm_count, cudaDevAttrMultiProcessorCount, device);
+  moe_status st = alloc_dense(x);
+  if (st != MOE_OK) {
+    delete x;
+    return st;
+  }
+  const size_t R = vocab, d = d_model;
+  cudaError_t e = cudaMemcpy(x->codes, w->codes, R * d / 2, cudaMemcpyDefault);
+  if (e == cudaSuccess) e = cudaMemcpy(x->scales, w->scales, R * d / 16, cudaMemcpyDefault);
+  if (e == cudaSuccess) e = cudaMemcpy(&x->ts[0], w->tensor_scale, sizeof(float), cudaMemcpyDefault);
+  return finish_init(x, e, out);
+}
+
+moe_status moe_head_forward(moe_dense* x, const void* x_bf16, int T, float* logits, cudaStream_t s) {
+  moe_status st = check_dense_call(x, x_bf16, T, logits);
+  if (st != MOE_OK) return st;
+  if (x->kind != 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  cudaSetDevice(x->device);
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x_bf16);
+  for (int t0 = 0; t0 < T; t0 += kTokPass) {
+    const int n = T - t0 < kTokPass ? T - t0 : kTokPass;
+    prep_x_kernel<<<kTokPass / 8, 256, 0, s>>>(xb + (size_t)t0 * x->d, n, x->d, x->x16, x->xun);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    GemvArgs g = base_args(x, n);
+    g.codes = x->codes;
+    g.scales = x->scales;
+    g.ntiles = x->rows / 16;
+    g.KS = x->d;
+    g.K = x->d;
+    g.b_hi = x->x16;
+    g.unshift = x->xun;
+    g.ts0 = x->ts[0];
+    g.out = logits + (size_t)t0 * x->rows;
+    g.out_ld = x->rows;
+    if (launch_gemv<kModeHead>(g, x->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_ffn_init(int d_model, int d_ff, const moe_matrix* gate, const moe_matrix* up, const moe_matrix* down,
+                        int max_tokens, int device, moe_dense** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (d_model <= 0 || d_ff <= 0 || max_tokens <= 0 || !matrix_ok(gate) || !matrix_ok(up) || !matrix_ok(down))
+    return MOE_ERR_INVALID_ARG;
+  if (!is_pow2_between(d_model, 256, 4096) || d_ff % 256 != 0 || d_ff > 65536 || max_tokens > 4096 ||
+      down_slices(d_ff) < 1)
+    return MOE_ERR_UNSUPPORTED;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return MOE_ERR_INVALID_ARG;
+  if (cudaSetDevice(device) != cudaSuccess) return MOE_ERR_CUDA;
+  moe_dense* x = new moe_dense();
+  x->kind = 1;
+  x->device = device;
+  x->d = d_model;
+  x->f = d_ff;
+  x->max_tokens = max_tokens;
+  x->S = down_slices(d_ff);
+  x->KS = d_ff / x->S;
+  cudaDeviceGetAttribute(&x->sm_count, cudaDevAttrMultiProcessorCount, device);
+  moe_status st = alloc_dense(x);
+  if (st != MOE_OK) {
+    delete x;
+    return st;
+  }
+  const size_t d = d_model, f = d_ff;
+  // canonical copies go through temporaries in the caller-independent part of the arena: the
+  // B-operand buffers are large enough only for small layers, so use one device temporary
+  uint8_t* tmp = nullptr;
+  const size_t tmp_bytes = 2 * f * d / 2;
+  cudaError_t e = device_alloc(reinterpret_cast<void**>(&tmp), tmp_bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(x->arena);
+    delete x;
+    return MOE_ERR_OOM;
+  }
+  // gate / up codes, then scales, into 8 + 8 row tiles
+  e = cudaMemcpy(tmp, gate->codes, f * d / 2, cudaMemcpyDefault);
+  if (e == cudaSuccess) e = cudaMemcpy(tmp + f * d / 2, up->codes, f * d / 2, cudaMemcpyDefault);
+  if (e == cudaSuccess) {
+    interleave_gu_kernel<<<(unsigned)(2 * f), 128>>>(tmp, tmp + f * d / 2, d / 2, (int)f, x->codes);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(tmp, gate->scales, f * d / 16, cudaMemcpyDefault);
+  if (e == cudaSuccess) e = cudaMemcpy(tmp + f * d / 16, up->scales, f * d / 16, cudaMemcpyDefault);
+  if (e == cudaSuccess) {
+    interleave_gu_kernel<<<(unsigned)(2 * f), 128>>>(tmp, tmp + f * d / 16, d / 16, (int)f, x->scales);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  // W_down into K slices
+  if (e == cudaSuccess) e = cudaMemcpy(tmp, down->codes, d * f / 2, cudaMemcpyDefault);
+  if (e == cudaSuccess) {
+    slice_rows_kernel<<<dim3((unsigned)d, (unsigned)x->S), 128>>>(tmp, (int)d, f / 2, x->S, x->dn_codes);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(tmp, down->scales, d * f / 16, cudaMemcpyDefault);
+  if (e == cudaSuccess) {
+    slice_rows_kernel<<<dim3((unsigned)d, (unsigned)x->S), 128>>>(tmp, (int)d, f / 16, x->S, x->dn_scales);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  cudaFree(tmp);
+  if (e == cudaSuccess) e = cudaMemcpy(&x->ts[0], gate->tensor_scale, sizeof(float), cudaMemcpyDefault);
+  if (e == cudaSuccess) e = cudaMemcpy(&x->ts[1], up->tensor_scale, sizeof(float), cudaMemcpyDefault);
+  if (e == cudaSuccess) e = cudaMemcpy(&x->ts[2], down->tensor_scale, sizeof(float), cudaMemcpyDefault);
+  return finish_init(x, e, out);
+}
+
+moe_status moe_ffn_forward(moe_dense* x, const void* x_bf16, int T, void* y_bf16, int residual, cudaStream_t s) {
+  moe_status st = check_dense_call(x, x_bf16, T, y_bf16);
+  if (st != MOE_OK) return st;
+  if (x->kind != 1 || (T > 0 && x_bf16 == y_bf16)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  cudaSetDevice(x->device);
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x_bf16);
+  __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y_bf16);
+  const int d = x->d, f = x->f;
+  for (int t0 = 0; t0 < T; t0 += kTokPass) {
+    const int n = T - t0 < kTokPass ? T - t0 : kTokPass;
+    prep_x_kernel<<<kTokPass / 8, 256, 0, s>>>(xb + (size_t)t0 * d, n, d, x->x16, x->xun);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    GemvArgs g = base_args(x, n);
+    g.codes = x->codes;
+    g.scales = x->scales;
+    g.ntiles = 2 * f / 16;
+    g.KS = d;
+    g.K = d;
+    g.b_hi = x->x16;
+    g.unshift = x->xun;
+    g.ts0 = x->ts[0];
+    g.ts1 = x->ts[1];
+    g.out = x->h;
+    g.out_ld = f;
+    if (launch_gemv<kModeGateUp>(g, x->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
+    prep_h_kernel<<<kTokPass / 8, 256, 0, s>>>(x->h, n, f, x->h_hi, x->h_lo, x->hun);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    GemvArgs dn = base_args(x, n);
+    dn.codes = x->dn_codes;
+    dn.scales = x->dn_scales;
+    dn.slice_codes = (size_t)d * x->KS / 2;
+    dn.slice_scales = (size_t)d * x->KS / 16;
+    dn.ntiles = d / 16;
+    dn.nslices = x->S;
+    dn.KS = x->KS;
+    dn.K = f;
+    dn.b_hi = x->h_hi;
+    dn.b_lo = x->h_lo;
+    dn.unshift = x->hun;
+    dn.ts0 = x->ts[2];
+    dn.out = x->part;
+    dn.out_ld = d;
+    if (launch_gemv<kModeDown>(dn, x->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
+    reduce_down_kernel<<<(n * d + 255) / 256, 256, 0, s>>>(x->part, x->S, n, d, xb + (size_t)t0 * d, residual,
+                                                         yb + (size_t)t0 * d);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_dense_get_device_status(moe_dense* x) {
+  if (!x) return MOE_ERR_INVALID_ARG;
+  cudaSetDevice(x->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, x->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(x->status, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status>(v);
+}
+
+moe_status moe_dense_destroy(moe_dense* x) {
+  if (!x) return MOE_OK;
+  cudaSetDevice(x->device);
+  cudaError_t e = cudaFree(x->arena);
+  delete x;
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -72,6 +72,8 @@ def lib():
                 "or_bucket": [vp, i, i, i, vp, vp, vp],
                 "or_expert": [ctypes.POINTER(_Layer), i, vp, i, i, vp, vp, i],
                 "or_moe_layer": [ctypes.POINTER(_Layer), vp, i, i, vp, vp, vp, vp, vp, vp, i],
+                "or_gemv": [vp, vp, ctypes.c_float, i, i, vp, i, vp, i],
+                "or_dense_ffn": [_Matrix, _Matrix, _Matrix, i, i, vp, i, vp, i],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -327,6 +329,29 @@ def route(x, router, bias, k: int, nthreads: int = 0) -> LayerResult:
     counts, _, _ = bucket(idx, logits.shape[1])
     return LayerResult(y=None, y_bf16=None, logits=logits, idx=idx, w=w, counts=counts,
                        near_tie=near_ties(logits, k))
+
+
+def gemv(codes, scales, ts, x, nthreads: int = 0) -> np.ndarray:
+    """Output layer: logits fp32 [T, R] = x [T, K] . W^T, W one NVFP4 tensor (codes [R, K/2])."""
+    codes, scales, x = _c(codes, np.uint8), _c(scales, np.uint8), _c(x, F32)
+    R, K = codes.shape[0], codes.shape[1] * 2
+    T = x.shape[0]
+    out = np.empty((T, R), F32)
+    lib().or_gemv(_p(codes), _p(scales), float(ts), R, K, _p(x), T, _p(out), nthreads)
+    return out
+
+
+def dense_ffn(gate, up, down, x, nthreads: int = 0) -> np.ndarray:
+    """Dense SwiGLU FFN: y fp32 [T, d]; gate/up = (codes [f, d/2], scales, ts), down = ([d, f/2], ...)."""
+    fix = lambda m: (_c(m[0], np.uint8), _c(m[1], np.uint8), np.array([m[2]], F32).reshape(1))  # noqa: E731
+    g, u, dn = fix(gate), fix(up), fix(down)
+    x = _c(x, F32)
+    T, d = x.shape
+    f = g[0].shape[0]
+    y = np.empty((T, d), F32)
+    mats = [_Matrix(*(_p(a) for a in m)) for m in (g, u, dn)]
+    lib().or_dense_ffn(mats[0], mats[1], mats[2], d, f, _p(x), T, _p(y), nthreads)
+    return y
 
 
 def residual(x, y) -> np.ndarray:

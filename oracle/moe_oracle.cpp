@@ -36,6 +36,11 @@
 //   expert        y_e = W_down (silu(W_gate x) * W_up x), silu(z) = z/(1+e^-z).
 //   combine       y = sum_j w_j y_{idx_j} + sum_s shared_s(x).
 //   prefill       x and h are quantised to NVFP4 (ts = 1) before their products.
+//   output layer  logits = W_head x with the 4-bit (NVFP4) head the OrcaRouter
+//                 page describes (section "量子化のレシピは最も転用しやすい部分です").
+//   dense layers  2 of the 49 layers are dense (section "このアーキテクチャは
+//                 メモリ帯域幅に関する主張である"); read as one SwiGLU FFN of
+//                 width d_ff in NVFP4, y = W_down (silu(W_gate x) * W_up x).
 //
 // Precision.  NVFP4 is dequantised to FP32 (e2m1*e4m3 is exact in fp32, the
 // multiplication by ts rounds once) and every value the layer passes from
@@ -186,12 +191,6 @@ void quantize_blocks(const float* w, int rows, int K, float ts, uint8_t* codes, 
   }
 }
 
-float tensor_scale(const float* w, size_t n) {
-  float amax = 0.f;
-  for (size_t i = 0; i < n; ++i) amax = std::max(amax, std::fabs(w[i]));
-  return amax / 2688.0f;
-}
-
 // fp32 values of an NVFP4 tensor: (e2m1 * e4m3) exactly, then * ts rounded once.
 void dequantize(const uint8_t* codes, const uint8_t* scales, float ts, int rows, int K, float* out) {
   const Tables& tb = tables();
@@ -315,10 +314,25 @@ void or_e2m1_encode(const float* v, long n, uint8_t* out) {
 void or_quantize(const float* w, int n, int rows, int K, uint8_t* codes, uint8_t* scales, float* ts,
                  int nthreads) {
   const size_t per = (size_t)rows * K;
-  parallel_for(n, nthreads, [&](long e) {
-    ts[e] = tensor_scale(w + e * per, per);
-    quantize_blocks(w + e * per, rows, K, ts[e], codes + e * per / 2, scales + e * per / 16);
-  });
+  for (int e = 0; e < n; ++e) {
+    // amax over the tensor (a maximum does not depend on the order), then rows in parallel
+    const float* we = w + e * per;
+    const long nchunk = std::min<long>(rows, 256);
+    std::vector<float> part(nchunk, 0.f);
+    parallel_for(nchunk, nthreads, [&](long c) {
+      const size_t r0 = (size_t)rows * c / nchunk, r1 = (size_t)rows * (c + 1) / nchunk;
+      float m = 0.f;
+      for (size_t i = r0 * K; i < r1 * K; ++i) m = std::max(m, std::fabs(we[i]));
+      part[c] = m;
+    });
+    float amax = 0.f;
+    for (long c = 0; c < nchunk; ++c) amax = std::max(amax, part[c]);
+    ts[e] = amax / 2688.0f;
+    parallel_for(rows, nthreads, [&](long r) {
+      quantize_blocks(we + (size_t)r * K, 1, K, ts[e], codes + e * per / 2 + (size_t)r * K / 2,
+                      scales + e * per / 16 + (size_t)r * K / 16);
+    });
+  }
 }
 
 // Activation quantiser (tensor scale 1): a [rows][K] -> codes, scales.
@@ -454,6 +468,33 @@ void or_moe_layer(const OrLayer* L, const float* x, int T, int prefill, const in
     std::vector<int32_t> offs(E + 1), perm((size_t)T * k);
     or_bucket(idx.data(), T, k, E, counts_out, offs.data(), perm.data());
   }
+}
+
+// Output layer: out [T][R] = x [T][K] . W^T for one NVFP4 matrix W [R][K].
+void or_gemv(const uint8_t* codes, const uint8_t* scales, float ts, int R, int K, const float* x, int T, float* out,
+             int nthreads) {
+  parallel_for(R, nthreads, [&](long r) {
+    std::vector<float> w(K);
+    dequantize(codes + (size_t)r * K / 2, scales + (size_t)r * K / 16, ts, 1, K, w.data());
+    for (int t = 0; t < T; ++t) out[(size_t)t * R + r] = dot(w.data(), x + (size_t)t * K, K);
+  });
+}
+
+// Dense SwiGLU FFN (one NVFP4 expert of width f, weight 1): y [T][d] fp32.
+void or_dense_ffn(OrMatrix gate, OrMatrix up, OrMatrix down, int d, int f, const float* x, int T, float* y,
+                  int nthreads) {
+  OrLayer L{};
+  L.d = d;
+  L.E = 1;
+  L.k = 1;
+  L.f = f;
+  L.S = 0;
+  L.gate = gate;
+  L.up = up;
+  L.down = down;
+  std::vector<std::pair<int, long>> pairs;
+  for (long t = 0; t < T; ++t) pairs.emplace_back(0, t);
+  run_pairs(&L, pairs, x, 0, nullptr, y, nthreads);
 }
 
 }  // extern "C"

@@ -18,8 +18,16 @@ layers; hidden size 2048 and expert width 512 are the stated assumptions):
   gets a Zipf rank r_e (a seeded permutation of 1..E) and the bias
   -beta * s * ln(r_e) with s = 1.1, beta = 0.1.
 
+* the output layer W_head [vocab, d] and the dense FFN layers (W_gate, W_up
+  [d_ff, d], W_down [d, d_ff]), fp32 ~ N(0, 0.02) like the experts.  Their
+  sizes are not on the pages; the readings: vocab 151,936 (the ~0.3B gap
+  between ~2.5B active including the output head and the ~2.2B active body,
+  at d = 2048) and d_ff 18,432 for each of the 2 dense layers (what the 39.8B
+  total and the ~2.2B active body leave for them).
+
 Seeds: weights of layer l use 1000 + l, the router of layer l uses 2000 + l,
-tokens of step i use 3000 + i; the tiny workload uses seed 0 throughout.
+tokens of step i use 3000 + i, dense layer l 5000 + l, the output layer 6000;
+the tiny workload uses seed 0 throughout.
 
 Generation uses ``torch.Generator`` on the requested device, so the same call
 on the same device always gives the same numbers.  CPU and CUDA generators
@@ -36,6 +44,7 @@ import torch
 __all__ = [
     "MoEShape", "TINY", "FLINT", "layer_seed", "router_seed", "token_seed",
     "expert_weights", "expert_weights_one", "router_weight", "zipf_bias", "tokens",
+    "FLINT_VOCAB", "FLINT_DENSE_FF", "dense_seed", "head_seed", "dense_ffn_weights", "head_weight",
 ]
 
 
@@ -57,6 +66,19 @@ class MoEShape:
 TINY = MoEShape(d_model=256, n_experts=16, top_k=2, d_ff=128, n_shared=1)
 #: Flint-shaped layer: d=2048, 256 experts top-6 + 1 shared, f=512
 FLINT = MoEShape(d_model=2048, n_experts=256, top_k=6, d_ff=512, n_shared=1)
+
+
+#: output-layer rows and dense-FFN width (readings of the pages' parameter counts)
+FLINT_VOCAB = 151_936
+FLINT_DENSE_FF = 18_432
+
+
+def dense_seed(layer: int) -> int:
+    return 5000 + layer
+
+
+def head_seed() -> int:
+    return 6000
 
 
 def layer_seed(layer: int) -> int:
@@ -106,6 +128,21 @@ def expert_weights_one(shape: MoEShape, seed: int, expert: int, device="cpu",
     w_up = torch.randn((f, d), generator=g, device=device, dtype=torch.float32).mul_(std)
     w_down = torch.randn((d, f), generator=g, device=device, dtype=torch.float32).mul_(std)
     return w_gate, w_up, w_down
+
+
+def dense_ffn_weights(d_model: int, d_ff: int, seed: int, device="cpu", std: float = 0.02):
+    """fp32 (W_gate [d_ff, d], W_up [d_ff, d], W_down [d, d_ff]) of one dense layer, in that order."""
+    g = _gen(seed, device)
+    w_gate = torch.randn((d_ff, d_model), generator=g, device=device, dtype=torch.float32).mul_(std)
+    w_up = torch.randn((d_ff, d_model), generator=g, device=device, dtype=torch.float32).mul_(std)
+    w_down = torch.randn((d_model, d_ff), generator=g, device=device, dtype=torch.float32).mul_(std)
+    return w_gate, w_up, w_down
+
+
+def head_weight(vocab: int, d_model: int, seed: int, device="cpu", std: float = 0.02):
+    """fp32 output-layer weight [vocab, d]."""
+    g = _gen(seed, device)
+    return torch.randn((vocab, d_model), generator=g, device=device, dtype=torch.float32).mul_(std)
 
 
 def router_weight(shape: MoEShape, seed: int, device="cpu", std: float = 0.02):

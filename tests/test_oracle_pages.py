@@ -10,7 +10,13 @@ and the weight format, not outputs:
 * the routed + shared experts of 47 layers at d=2048, f=512 fit inside the
   39.8B total, and the active experts plus attention stay within the ~2.2B
   active body;
-* "71% smaller" is 1 - 22.86 / 79.59.
+* "71% smaller" is 1 - 22.86 / 79.59;
+* the readings of the two sizes the pages leave open -- the output layer's
+  vocabulary (151,936 rows at d = 2048) and the dense layers' width (18,432)
+  -- fit the counts: ~2.5B active with the head minus ~2.2B without it is the
+  head, and what the 39.8B total and the ~2.2B active body leave after the
+  experts, routers, attention and (untied) embedding and head is the two
+  dense SwiGLU FFNs, each within the rounding of the printed figures.
 """
 import os
 
@@ -70,3 +76,25 @@ def test_layer_shape_fits_parameter_budget():
     assert active <= f["active_body_billion"] * 1e9 * 1.05
     # NVFP4 bytes of one expert: codes + one E4M3 byte per 16 elements
     assert per_expert // 2 + per_expert // 16 == 1_769_472
+
+
+def test_head_and_dense_widths_fit_page_counts():
+    import synth
+    f = _figures()
+    d = 2048
+    head = synth.FLINT_VOCAB * d
+    assert abs(head - (f["active_with_head_billion"] - f["active_body_billion"]) * 1e9) <= 0.1e9
+    per_expert = 3 * d * 512
+    n_moe = int(f["layers_moe"])
+    n_dense = int(f["layers_total"]) - n_moe
+    hd = f["head_dim"]
+    attn = f["layers_total"] * (d * f["query_heads"] * hd * 2 + d * f["kv_heads"] * hd * 2)
+    routers = n_moe * d * f["routed_experts_per_layer"]
+    dense = n_dense * 3 * d * synth.FLINT_DENSE_FF
+    left_total = (f["params_total_billion"] * 1e9
+                  - n_moe * (f["routed_experts_per_layer"] + f["shared_experts"]) * per_expert
+                  - routers - attn - 2 * head)
+    left_active = (f["active_body_billion"] * 1e9
+                   - n_moe * (f["experts_per_token"] + f["shared_experts"]) * per_expert - routers - attn)
+    assert abs(dense - left_total) <= 0.05e9, (dense, left_total)
+    assert abs(dense - left_active) <= 0.05e9, (dense, left_active)

@@ -323,3 +323,33 @@ def test_cpp_layer_agrees_with_numpy_oracle(prefill):
     assert np.allclose(a.w, b.w, rtol=3e-7, atol=0)
     rel = np.linalg.norm(a.y - b.y) / np.linalg.norm(b.y)
     assert rel < (1e-6 if not prefill else 1e-5), rel
+
+
+# --------------------------------------------------------------------------
+# output layer and dense FFN (C++ oracle)
+# --------------------------------------------------------------------------
+def test_cpp_gemv_against_fsum_loops():
+    rng = np.random.default_rng(45)
+    w = (rng.standard_normal((24, 64)) * 0.1).astype(F32)
+    c, s, ts = cpp.quantize(w)
+    wq = cpp.dequantize(c, s, ts).astype(np.float64)
+    x = nvfp4.bf16_rne(rng.standard_normal((3, 64))).astype(F32)
+    got = cpp.gemv(c, s, ts, x, nthreads=3)
+    for t in range(3):
+        for r in range(24):
+            ref = math.fsum(float(wq[r, k]) * float(x[t, k]) for k in range(64))
+            assert abs(float(got[t, r]) - ref) <= float(np.spacing(F32(abs(ref))))
+
+
+def test_cpp_dense_ffn_against_textbook_loops():
+    rng = np.random.default_rng(46)
+    d, f = 32, 48
+    mats = [cpp.quantize((rng.standard_normal(shape) * 0.2).astype(F32)) for shape in ((f, d), (f, d), (d, f))]
+    x = nvfp4.bf16_rne(rng.standard_normal((2, d))).astype(F32)
+    y = cpp.dense_ffn(mats[0], mats[1], mats[2], x)
+    wg, wu, wd = (cpp.dequantize(*m).tolist() for m in mats)
+    for t in range(2):
+        h = _textbook_h(wg, wu, x[t].tolist(), round32=True)
+        ref = np.array([math.fsum(wd[r][j] * h[j] for j in range(f)) for r in range(d)])
+        ulp = np.spacing(np.abs(ref).astype(F32)).astype(np.float64)
+        assert np.all(np.abs(y[t] - ref) <= 2 * ulp)
