@@ -516,7 +516,9 @@ def run_dense(args):
     with torch.cuda.graph(g, stream=stream):
         for i in range(chunk):
             step(i)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(chunk)]
+    # external events: recorded inside the capture as event-record nodes that can be timed
+    ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+          for _ in range(chunk)]
     for a, b in ev:
         a.record(stream)
         b.record(stream)

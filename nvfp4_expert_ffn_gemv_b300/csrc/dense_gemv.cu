@@ -11,8 +11,9 @@
 //
 //   * persistent CTAs, one per SM; the matrix is cut into units of 16 rows x
 //     one K slice, unit u going to CTA u % grid;
-//   * warp 0 streams units with TMA bulk copies (codes and E4M3 scales of a
-//     unit are contiguous) into a ring of up to 8 shared-memory stages;
+//   * warp 0 streams units with TMA bulk copies (the codes and the E4M3 scales
+//     of a unit are contiguous, stored swizzled so that the consumers' reads
+//     are free of bank conflicts) into a ring of up to 8 shared-memory stages;
 //     consumer warp w owns stage w, so a stage is refilled as soon as its
 //     warp is done with it and ~150 KB per SM stay in flight;
 //   * the consumer multiplies on the tensor cores (mma.sync m16n8k16, f16 in,
@@ -64,25 +65,70 @@ struct GemvArgs {
 
 __device__ __forceinline__ uint2 ldg64(const uint8_t* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
 
+// Stage layout of one unit: the 16 code rows (KS/2 bytes each, a multiple of
+// 128) and then the 16 scale rows (KS/16 bytes each), as one bulk copy each.
+// The weights are stored swizzled (see swizzle_rows_kernel): inside every
+// 128-byte segment of row r, 16-byte granule i sits at granule i ^ m(r % 8),
+// m(r) = 4 (r & 1) + (r >> 1).  A quarter-warp's 16-byte code loads cover
+// granules {0..3} (or {4..7}) of the two rows 2i and 2i + 1, whose masks
+// differ in bit 2, so they land on disjoint banks; the 8 rows of the 2-byte
+// scale loads land on 8 different granules.  Scale rows are swizzled the same
+// way when their length is a multiple of 128 bytes.
+__host__ __device__ __forceinline__ uint32_t stage_bytes_of(int KS) { return 16u * ((uint32_t)KS / 2 + (uint32_t)KS / 16); }
+
+__host__ __device__ __forceinline__ int swz_mask(int r8) { return ((r8 & 1) << 2) | (r8 >> 1); }
+
+__device__ __forceinline__ int swz(int byte, int row8) {
+  return (byte & ~0x7F) | ((((byte >> 4) & 7) ^ swz_mask(row8)) << 4) | (byte & 15);
+}
+
+// One unit (16 rows x one K slice) by a pair of warps: warp `half` multiplies
+// the chunks of its half of the K slice.  The MMAs are spread over CH
+// independent accumulator chains (by k step), so the latency of one chain does
+// not serialise the unit; the down projection sends the hi and lo halves of h
+// to separate chains as well.  The second warp of the pair hands its sums to
+// the first through `xch` (the caller's named barrier in between); the first
+// adds them and runs the epilogue.
 template <int MODE, int NG>
 __device__ __forceinline__ void consume_unit(const GemvArgs& g, const uint8_t* sc, const uint8_t* ss, int slice,
-                                             int tile) {
+                                             int tile, int half, float* xch, int bar_id) {
+  constexpr int CH = NG >= 4 ? 1 : (NG == 2 ? 2 : 4);
   const int lane = threadIdx.x & 31, gq = lane >> 2, c = lane & 3;
-  const int KS = g.KS, CB = KS / 2, SB = KS / 16;
-  float acc[NG][4];
+  const int KS = g.KS;
+  const int CB = KS / 2, SB = KS / 16;
+  const bool sswz = (SB & 127) == 0;     // scale rows swizzled too
+  float acc[CH][NG][4];
+  float accl[MODE == kModeDown ? CH : 1][MODE == kModeDown ? NG : 1][4];
 #pragma unroll
-  for (int q = 0; q < NG; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-  const uint8_t* row0 = sc + gq * CB + c * 16;
+  for (int h = 0; h < CH; ++h)
+#pragma unroll
+    for (int q = 0; q < NG; ++q) {
+      acc[h][q][0] = acc[h][q][1] = acc[h][q][2] = acc[h][q][3] = 0.f;
+      if (MODE == kModeDown) accl[h][q][0] = accl[h][q][1] = accl[h][q][2] = accl[h][q][3] = 0.f;
+    }
+  const uint8_t* row0 = sc + gq * CB;
   const uint8_t* row8 = row0 + 8 * CB;
-  const uint8_t* srow0 = ss + gq * SB + c * 2;
+  const uint8_t* srow0 = ss + gq * SB;
   const uint8_t* srow8 = srow0 + 8 * SB;
   const size_t brow = (size_t)g.K * 2;
   const int k0 = slice * KS;     // first k of this unit in the B operand
-  for (int ch = 0; ch < KS / 128; ++ch) {
-    const uint4 wc = *reinterpret_cast<const uint4*>(row0 + ch * 64);
-    const uint4 wc8 = *reinterpret_cast<const uint4*>(row8 + ch * 64);
-    const uint32_t s2 = cvt_e4m3x2_f16x2(*reinterpret_cast<const uint16_t*>(srow0 + ch * 8));
-    const uint32_t s28 = cvt_e4m3x2_f16x2(*reinterpret_cast<const uint16_t*>(srow8 + ch * 8));
+  const int nch = KS / 128, ch0 = half ? nch / 2 : 0, ch1 = half ? nch : nch / 2;
+  // the next chunk's code words and scales are loaded one chunk ahead
+  auto load_a = [&](int ch, uint4& w, uint4& w8, uint32_t& sr, uint32_t& sr8) {
+    const int cb = swz(ch * 64 + c * 16, gq);                       // rows gq and gq + 8: same r % 8
+    const int sb = sswz ? swz(ch * 8 + c * 2, gq) : ch * 8 + c * 2;
+    w = *reinterpret_cast<const uint4*>(row0 + cb);
+    w8 = *reinterpret_cast<const uint4*>(row8 + cb);
+    sr = *reinterpret_cast<const uint16_t*>(srow0 + sb);
+    sr8 = *reinterpret_cast<const uint16_t*>(srow8 + sb);
+  };
+  uint4 nwc, nwc8;
+  uint32_t nsr, nsr8;
+  load_a(ch0, nwc, nwc8, nsr, nsr8);
+  for (int ch = ch0; ch < ch1; ++ch) {
+    const uint4 wc = nwc, wc8 = nwc8;
+    const uint32_t s2 = cvt_e4m3x2_f16x2(nsr), s28 = cvt_e4m3x2_f16x2(nsr8);
+    if (ch + 1 < ch1) load_a(ch + 1, nwc, nwc8, nsr, nsr8);
     const size_t boff = (size_t)(k0 + ch * 128) * 2;
 #pragma unroll
     for (int wd = 0; wd < 4; ++wd) {
@@ -93,19 +139,49 @@ __device__ __forceinline__ void consume_unit(const GemvArgs& g, const uint8_t* s
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         const int kk = 2 * wd + h2;
+        const int chn = kk % CH;
 #pragma unroll
         for (int q = 0; q < NG; ++q) {
+          // B column gq of group q is token 8q + gq: lanes past the batch feed zeros without a load
+          const bool live = 8 * q + gq < g.T;
           const size_t off = (size_t)(8 * q + gq) * brow + boff + perm_off(c, kk);
-          const uint2 b = ldg64(g.b_hi + off);
-          mma_f16(acc[q], afp[h2], b.x, b.y);
+          const uint2 b = live ? ldg64(g.b_hi + off) : make_uint2(0u, 0u);
+          mma_f16(acc[chn][q], afp[h2], b.x, b.y);
           if (MODE == kModeDown) {
-            const uint2 bl = ldg64(g.b_lo + off);
-            mma_f16(acc[q], afp[h2], bl.x, bl.y);
+            const uint2 bl = live ? ldg64(g.b_lo + off) : make_uint2(0u, 0u);
+            mma_f16(accl[chn % (MODE == kModeDown ? CH : 1)][q % (MODE == kModeDown ? NG : 1)], afp[h2], bl.x, bl.y);
           }
         }
       }
     }
   }
+#pragma unroll
+  for (int h = 1; h < CH; ++h)
+#pragma unroll
+    for (int q = 0; q < NG; ++q)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[0][q][i] += acc[h][q][i];
+  if (MODE == kModeDown) {
+#pragma unroll
+    for (int h = 0; h < CH; ++h)
+#pragma unroll
+      for (int q = 0; q < NG; ++q)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[0][q][i] += accl[h % (MODE == kModeDown ? CH : 1)][q % (MODE == kModeDown ? NG : 1)][i];
+  }
+  // the pair's sums meet: the second warp writes, the first adds (fixed order: first + second)
+  if (half) {
+#pragma unroll
+    for (int q = 0; q < NG; ++q)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xch[(q * 4 + i) * 32 + lane] = acc[0][q][i];
+  }
+  asm volatile("bar.sync %0, 64;" :: "r"(bar_id) : "memory");
+  if (half) return;
+#pragma unroll
+  for (int q = 0; q < NG; ++q)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[0][q][i] += xch[(q * 4 + i) * 32 + lane];
   // lanes hold rows gq (acc 0, 1) and gq + 8 (acc 2, 3) of the tile, tokens 8q + 2c, 8q + 2c + 1
 #pragma unroll
   for (int q = 0; q < NG; ++q) {
@@ -116,28 +192,30 @@ __device__ __forceinline__ void consume_unit(const GemvArgs& g, const uint8_t* s
       const float un = g.unshift[t];
       if (MODE == kModeHead) {
         const int r = tile * 16 + gq;
-        g.out[(size_t)t * g.out_ld + r] = acc[q][j] * g.ts0 * un;
-        g.out[(size_t)t * g.out_ld + r + 8] = acc[q][2 + j] * g.ts0 * un;
+        g.out[(size_t)t * g.out_ld + r] = acc[0][q][j] * g.ts0 * un;
+        g.out[(size_t)t * g.out_ld + r + 8] = acc[0][q][2 + j] * g.ts0 * un;
       } else if (MODE == kModeGateUp) {
-        const float gv = acc[q][j] * g.ts0 * un, uv = acc[q][2 + j] * g.ts1 * un;
+        const float gv = acc[0][q][j] * g.ts0 * un, uv = acc[0][q][2 + j] * g.ts1 * un;
         g.out[(size_t)t * g.out_ld + tile * 8 + gq] = silu_f(gv) * uv;
       } else {
         float* dst = g.out + ((size_t)slice * g.T + t) * g.out_ld + tile * 16 + gq;
-        dst[0] = acc[q][j] * g.ts0 * un;
-        dst[8] = acc[q][2 + j] * g.ts0 * un;
+        dst[0] = acc[0][q][j] * g.ts0 * un;
+        dst[8] = acc[0][q][2 + j] * g.ts0 * un;
       }
     }
   }
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(32 * (kMaxStages + 1), 1) nvfp4_gemv_kernel(GemvArgs g) {
+__global__ void __launch_bounds__(32 * (2 * kMaxStages + 1), 1) nvfp4_gemv_kernel(GemvArgs g) {
   extern __shared__ __align__(128) uint8_t gsm[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+  // partial sums a warp pair exchanges: [stage][unit parity][16 values][32 lanes]
+  __shared__ float xch_all[kMaxStages][2][16 * 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = g.nstages;
-  const uint32_t ucodes = 16u * (uint32_t)g.KS / 2, uscales = 16u * (uint32_t)g.KS / 16;
-  const uint32_t stage_bytes = ucodes + uscales;
+  const uint32_t rcodes = (uint32_t)g.KS / 2, rscales = (uint32_t)g.KS / 16;     // bytes per row
+  const uint32_t stage_bytes = stage_bytes_of(g.KS), scale_off = 16 * rcodes;
   const int units = g.ntiles * g.nslices;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -157,27 +235,30 @@ __global__ void __launch_bounds__(32 * (kMaxStages + 1), 1) nvfp4_gemv_kernel(Ge
         const int slice = u / g.ntiles, tile = u % g.ntiles;
         uint8_t* dst = gsm + (size_t)s * stage_bytes;
         mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
-        bulk_load(dst, g.codes + slice * g.slice_codes + (size_t)tile * ucodes, ucodes, &full_bar[s]);
-        bulk_load(dst + ucodes, g.scales + slice * g.slice_scales + (size_t)tile * uscales, uscales, &full_bar[s]);
+        bulk_load(dst, g.codes + slice * g.slice_codes + (size_t)tile * 16 * rcodes, 16 * rcodes, &full_bar[s]);
+        bulk_load(dst + scale_off, g.scales + slice * g.slice_scales + (size_t)tile * 16 * rscales, 16 * rscales,
+                  &full_bar[s]);
       }
-      // every copy issued here lands before the consumer that owns its stage
-      // finishes, and the CTA leaves only after all consumers (below)
     }
-  } else if (warp - 1 < NS) {
-    const int s = warp - 1;
+    // every copy issued here lands before the consumer that owns its stage
+    // finishes, and the CTA leaves only after all consumers (below)
+  } else if (warp - 1 < 2 * NS) {
+    // warps 2s + 1 and 2s + 2 share stage s, each on one half of the K slice
+    const int s = (warp - 1) >> 1, half = (warp - 1) & 1;
     int j = s;
     for (int u = blockIdx.x + s * gridDim.x; u < units; u += NS * gridDim.x, j += NS) {
       if (!wait_parity(&full_bar[s], (j / NS) & 1)) { ok = false; }
       const uint8_t* sc = gsm + (size_t)s * stage_bytes;
       const int slice = u / g.ntiles, tile = u % g.ntiles;
-      if (ok) {
-        const int ngroups = (g.T + 7) / 8;
-        if (ngroups <= 1) consume_unit<MODE, 1>(g, sc, sc + ucodes, slice, tile);
-        else if (ngroups == 2) consume_unit<MODE, 2>(g, sc, sc + ucodes, slice, tile);
-        else consume_unit<MODE, 4>(g, sc, sc + ucodes, slice, tile);
-      }
+      // both warps of the pair take the same branch (the wait outcome is shared through the
+      // barrier count only when both run): a failed wait skips the work but keeps the barrier
+      const int ngroups = (g.T + 7) / 8;
+      float* xch = xch_all[s][(j / NS) & 1];
+      if (ngroups <= 1) consume_unit<MODE, 1>(g, sc, sc + scale_off, slice, tile, half, xch, s + 1);
+      else if (ngroups == 2) consume_unit<MODE, 2>(g, sc, sc + scale_off, slice, tile, half, xch, s + 1);
+      else consume_unit<MODE, 4>(g, sc, sc + scale_off, slice, tile, half, xch, s + 1);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[s]);
+      if (lane == 0 && half == 0) mbar_arrive(&empty_bar[s]);
     }
   }
   if (!ok) latch_status(g.status, MOE_ERR_TIMEOUT);
@@ -185,31 +266,46 @@ __global__ void __launch_bounds__(32 * (kMaxStages + 1), 1) nvfp4_gemv_kernel(Ge
   if (threadIdx.x == 0 && (g.dbg & MOE_DEBUG_FORCE_TIMEOUT)) latch_status(g.status, MOE_ERR_TIMEOUT);
 }
 
-// bf16 x [T][K] -> prescaled f16 in the permuted chunk order, kTokPass rows
-// (rows T.. zero), one warp per row; unshift[t] = 2^-shift.
+// Rows of the B operand a pass over T tokens reads: whole groups of 8 tokens
+// (1, 2 or 4 groups).
+__host__ __device__ __forceinline__ int rows_read(int T) {
+  const int ng = (T + 7) / 8;
+  return ng <= 2 ? 8 * ng : kTokPass;
+}
+
+// Block-wide maximum of non-negative floats (as ordered bit patterns) of 256 threads.
+__device__ __forceinline__ float block_max256(float m, uint32_t* red) {
+  const uint32_t w = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = w;
+  __syncthreads();
+  const uint32_t v = __reduce_max_sync(0xffffffffu, red[threadIdx.x & 7]);   // every warp sees all 8
+  return __uint_as_float(v);
+}
+
+// bf16 x [T][K] -> prescaled f16 in the permuted chunk order, one CTA per row
+// of the B operand (rows T .. rows_read(T) - 1 zero); unshift[t] = 2^-shift.
 __global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int K,
                                                      uint8_t* __restrict__ out, float* __restrict__ unshift) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= kTokPass) return;
+  __shared__ uint32_t red[8];
+  const int t = blockIdx.x;
   uint8_t* dst = out + (size_t)t * K * 2;
   if (t >= T) {
-    for (int i = lane; i < K / 8; i += 32) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (lane == 0) unshift[t] = 0.f;
+    for (int i = threadIdx.x; i < K / 8; i += 256) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) unshift[t] = 0.f;
     return;
   }
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * K);
   float m = 0.f;
-  for (int i = lane; i < K / 8; i += 32) {
+  for (int i = threadIdx.x; i < K / 8; i += 256) {
     const uint4 v = __ldg(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
   }
-  const int shift = prescale_shift(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+  const int shift = prescale_shift(__float_as_uint(block_max256(m, red)));
   const float sc = pow2i(shift);
-  for (int i = lane; i < K / 8; i += 32) {
+  for (int i = threadIdx.x; i < K / 8; i += 256) {
     const uint4 v = __ldg(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t hv[4];
@@ -223,34 +319,33 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* __rest
     *reinterpret_cast<uint2*>(base + perm_off(cc, kk)) = make_uint2(hv[0], hv[1]);
     *reinterpret_cast<uint2*>(base + perm_off(cc, kk + 1)) = make_uint2(hv[2], hv[3]);
   }
-  if (lane == 0) unshift[t] = pow2i(-shift);
+  if (threadIdx.x == 0) unshift[t] = pow2i(-shift);
 }
 
-// fp32 h [T][K] -> prescaled f16 hi + lo in the permuted chunk order (rows T.. zero).
+// fp32 h [T][K] -> prescaled f16 hi + lo in the permuted chunk order, one CTA per row (rows T.. zero).
 __global__ void __launch_bounds__(256) prep_h_kernel(const float* __restrict__ h, int T, int K, uint8_t* __restrict__ hi,
                                                      uint8_t* __restrict__ lo, float* __restrict__ unshift) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= kTokPass) return;
+  __shared__ uint32_t red[8];
+  const int t = blockIdx.x;
   uint8_t* dh = hi + (size_t)t * K * 2;
   uint8_t* dl = lo + (size_t)t * K * 2;
   if (t >= T) {
-    for (int i = lane; i < K / 8; i += 32) {
+    for (int i = threadIdx.x; i < K / 8; i += 256) {
       reinterpret_cast<uint4*>(dh)[i] = make_uint4(0u, 0u, 0u, 0u);
       reinterpret_cast<uint4*>(dl)[i] = make_uint4(0u, 0u, 0u, 0u);
     }
-    if (lane == 0) unshift[t] = 0.f;
+    if (threadIdx.x == 0) unshift[t] = 0.f;
     return;
   }
   const float4* src = reinterpret_cast<const float4*>(h + (size_t)t * K);
   float m = 0.f;
-  for (int i = lane; i < K / 4; i += 32) {
+  for (int i = threadIdx.x; i < K / 4; i += 256) {
     const float4 v = src[i];
     m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
   }
-  const int shift = prescale_shift(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+  const int shift = prescale_shift(__float_as_uint(block_max256(m, red)));
   const float sc = pow2i(shift);
-  for (int i = lane; i < K / 4; i += 32) {
+  for (int i = threadIdx.x; i < K / 4; i += 256) {
     const float4 v = src[i];
     uint2 vh, vl;
     split_hi_lo(v.x * sc, v.y * sc, v.z * sc, v.w * sc, vh, vl);
@@ -259,7 +354,7 @@ __global__ void __launch_bounds__(256) prep_h_kernel(const float* __restrict__ h
     *reinterpret_cast<uint2*>(dh + off) = vh;
     *reinterpret_cast<uint2*>(dl + off) = vl;
   }
-  if (lane == 0) unshift[t] = pow2i(-shift);
+  if (threadIdx.x == 0) unshift[t] = pow2i(-shift);
 }
 
 // y[t][r] = bf16(sum over the S K slices, in order, of partial[s][t][r] (+ x[t][r]))
@@ -272,6 +367,26 @@ __global__ void __launch_bounds__(256) reduce_down_kernel(const float* __restric
   for (int s = 0; s < S; ++s) acc += part[(size_t)s * T * d + i];
   if (residual) acc += __bfloat162float(x[i]);
   y[i] = __float2bfloat16_rn(acc);
+}
+
+// In place, one block per row of row_bytes (a multiple of 128): granule i of
+// every 128-byte segment of row r moves to granule i ^ m(r % 8).
+__global__ void swizzle_rows_kernel(uint8_t* __restrict__ buf, size_t row_bytes) {
+  extern __shared__ __align__(16) uint8_t row_sm[];
+  const size_t r = blockIdx.x;
+  uint4* row = reinterpret_cast<uint4*>(buf + r * row_bytes);
+  uint4* tmp = reinterpret_cast<uint4*>(row_sm);
+  const int n = (int)(row_bytes / 16);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) tmp[i] = row[i];
+  __syncthreads();
+  const int m = swz_mask((int)(r & 7));
+  for (int i = threadIdx.x; i < n; i += blockDim.x) row[(i & ~7) | ((i & 7) ^ m)] = tmp[i];
+}
+
+cudaError_t swizzle_rows(uint8_t* buf, size_t rows, size_t row_bytes) {
+  if (row_bytes % 128 != 0 || rows == 0) return cudaSuccess;
+  swizzle_rows_kernel<<<(unsigned)rows, 128, row_bytes>>>(buf, row_bytes);
+  return cudaGetLastError();
 }
 
 // gate/up [f][K] canonical -> tiles of 8 gate rows then the matching 8 up rows
@@ -293,19 +408,18 @@ __global__ void slice_rows_kernel(const uint8_t* __restrict__ src, int d, size_t
 }
 
 int stages_for(int KS) {
-  const int stage = 16 * KS / 2 + 16 * KS / 16;
-  int n = kStageBudget / stage;
+  int n = kStageBudget / (int)stage_bytes_of(KS);
   return n > kMaxStages ? kMaxStages : n;
 }
 
-size_t gemv_smem(int KS) { return (size_t)stages_for(KS) * (16 * KS / 2 + 16 * KS / 16); }
+size_t gemv_smem(int KS) { return (size_t)stages_for(KS) * stage_bytes_of(KS); }
 
 template <int MODE>
 cudaError_t launch_gemv(GemvArgs g, int sm_count, cudaStream_t s) {
   const int units = g.ntiles * g.nslices;
   const int grid = units < sm_count ? units : sm_count;
   g.nstages = stages_for(g.KS);
-  nvfp4_gemv_kernel<MODE><<<grid, 32 * (g.nstages + 1), gemv_smem(g.KS), s>>>(g);
+  nvfp4_gemv_kernel<MODE><<<grid, 32 * (2 * g.nstages + 1), gemv_smem(g.KS), s>>>(g);
   return cudaGetLastError();
 }
 
@@ -463,6 +577,8 @@ moe_status moe_head_init(int vocab, int d_model, const moe_matrix* w, int max_to
   cudaError_t e = cudaMemcpy(x->codes, w->codes, R * d / 2, cudaMemcpyDefault);
   if (e == cudaSuccess) e = cudaMemcpy(x->scales, w->scales, R * d / 16, cudaMemcpyDefault);
   if (e == cudaSuccess) e = cudaMemcpy(&x->ts[0], w->tensor_scale, sizeof(float), cudaMemcpyDefault);
+  if (e == cudaSuccess) e = swizzle_rows(x->codes, R, d / 2);
+  if (e == cudaSuccess) e = swizzle_rows(x->scales, R, d / 16);
   return finish_init(x, e, out);
 }
 
@@ -475,7 +591,7 @@ moe_status moe_head_forward(moe_dense* x, const void* x_bf16, int T, float* logi
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x_bf16);
   for (int t0 = 0; t0 < T; t0 += kTokPass) {
     const int n = T - t0 < kTokPass ? T - t0 : kTokPass;
-    prep_x_kernel<<<kTokPass / 8, 256, 0, s>>>(xb + (size_t)t0 * x->d, n, x->d, x->x16, x->xun);
+    prep_x_kernel<<<rows_read(n), 256, 0, s>>>(xb + (size_t)t0 * x->d, n, x->d, x->x16, x->xun);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     GemvArgs g = base_args(x, n);
     g.codes = x->codes;
@@ -560,6 +676,10 @@ moe_status moe_ffn_init(int d_model, int d_ff, const moe_matrix* gate, const moe
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   cudaFree(tmp);
+  if (e == cudaSuccess) e = swizzle_rows(x->codes, 2 * f, d / 2);
+  if (e == cudaSuccess) e = swizzle_rows(x->scales, 2 * f, d / 16);
+  if (e == cudaSuccess) e = swizzle_rows(x->dn_codes, (size_t)x->S * d, x->KS / 2);
+  if (e == cudaSuccess) e = swizzle_rows(x->dn_scales, (size_t)x->S * d, x->KS / 16);
   if (e == cudaSuccess) e = cudaMemcpy(&x->ts[0], gate->tensor_scale, sizeof(float), cudaMemcpyDefault);
   if (e == cudaSuccess) e = cudaMemcpy(&x->ts[1], up->tensor_scale, sizeof(float), cudaMemcpyDefault);
   if (e == cudaSuccess) e = cudaMemcpy(&x->ts[2], down->tensor_scale, sizeof(float), cudaMemcpyDefault);
@@ -577,7 +697,7 @@ moe_status moe_ffn_forward(moe_dense* x, const void* x_bf16, int T, void* y_bf16
   const int d = x->d, f = x->f;
   for (int t0 = 0; t0 < T; t0 += kTokPass) {
     const int n = T - t0 < kTokPass ? T - t0 : kTokPass;
-    prep_x_kernel<<<kTokPass / 8, 256, 0, s>>>(xb + (size_t)t0 * d, n, d, x->x16, x->xun);
+    prep_x_kernel<<<rows_read(n), 256, 0, s>>>(xb + (size_t)t0 * d, n, d, x->x16, x->xun);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     GemvArgs g = base_args(x, n);
     g.codes = x->codes;
@@ -592,7 +712,7 @@ moe_status moe_ffn_forward(moe_dense* x, const void* x_bf16, int T, void* y_bf16
     g.out = x->h;
     g.out_ld = f;
     if (launch_gemv<kModeGateUp>(g, x->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
-    prep_h_kernel<<<kTokPass / 8, 256, 0, s>>>(x->h, n, f, x->h_hi, x->h_lo, x->hun);
+    prep_h_kernel<<<rows_read(n), 256, 0, s>>>(x->h, n, f, x->h_hi, x->h_lo, x->hun);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     GemvArgs dn = base_args(x, n);
     dn.codes = x->dn_codes;
