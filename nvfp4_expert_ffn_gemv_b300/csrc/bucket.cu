@@ -209,8 +209,12 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T
     }
     r.slot_pos[s] = p;
     r.pos_tok[p] = t;
+    r.pos_w[p] = r.w[s];
   }
-  for (int q = threadIdx.x; q < S * T; q += blockDim.x) r.pos_tok[T * k + q] = q % T;
+  for (int q = threadIdx.x; q < S * T; q += blockDim.x) {
+    r.pos_tok[T * k + q] = q % T;
+    r.pos_w[T * k + q] = 1.f;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -321,9 +325,11 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(Routing r, int T, i
                   __ldg(r.chunk_cnt + (size_t)(t >> 5) * E + e) + __ldg(r.rank + s);
     r.slot_pos[s] = p;
     r.pos_tok[p] = t;
+    r.pos_w[p] = __ldg(r.w + s);
   } else if (s < T * k + S * T) {
     const int q = s - T * k;
     r.pos_tok[T * k + q] = q % T;
+    r.pos_w[T * k + q] = 1.f;
   }
 }
 

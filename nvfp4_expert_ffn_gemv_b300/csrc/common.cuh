@@ -124,6 +124,7 @@ struct Routing {
   int32_t* offsets;    // [E+1]
   int32_t* slot_pos;   // [T*k] slot -> position
   int32_t* pos_tok;    // [T*k + S*T] position -> token
+  float* pos_w;        // [T*k + S*T] position -> combine weight (1 for shared experts)
   int32_t* act_e;      // [E+S] active experts (count > 0), shared last
   int32_t* act_pos;    // [E+S] first position of each active expert
   int32_t* act_n;      // [E+S] tokens of each active expert

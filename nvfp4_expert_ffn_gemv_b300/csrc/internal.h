@@ -35,7 +35,8 @@ struct moe_ctx {
   float* router_partial = nullptr;
   nvmoe::Routing r{};
   float* h = nullptr;        // [P][f] fp32, P = T*k + S*T positions
-  float* yexp = nullptr;     // [P][d] fp32 per-position expert outputs
+  float* yexp = nullptr;     // [P][d] fp32 per-position expert outputs (batched decode)
+  float* yacc = nullptr;     // [max_tokens][d] fp32 prefill accumulator of the weighted expert outputs
   int* status = nullptr;     // device status word
   int max_positions = 0;
 
@@ -121,10 +122,13 @@ bool mma_decode_supported(const moe_config& c);
 cudaError_t prepare_mma_decode(const moe_ctx* c);
 cudaError_t launch_mma_decode(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
 bool prefill_supported(const moe_config& c);
+bool prefill_accumulates(const moe_config& c, int T);
 size_t prefill_max_rows(const moe_config& c);
 cudaError_t prefill_prepare(moe_ctx* c);
 cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
 cudaError_t launch_gather_prefill_h(const moe_ctx* c, int T, uint8_t* codes, uint8_t* sf, cudaStream_t s);
+cudaError_t launch_prefill_finish(const moe_ctx* c, const __nv_bfloat16* x, int T, __nv_bfloat16* y, int residual,
+                                  cudaStream_t s);
 bool b1_supported(const moe_config& c);
 bool b1_plan(const moe_config& c, int sm_count, int ctas_per_sm, int* grid, int* rmax, int* nbmax, size_t* smem);
 size_t b1_row_bytes(int d);

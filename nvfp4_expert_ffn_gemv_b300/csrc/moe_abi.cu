@@ -68,6 +68,7 @@ size_t carve(moe_ctx* x, uint8_t* base) {
   x->r.offsets = cv.take<int32_t>(base, E + 1);
   x->r.slot_pos = cv.take<int32_t>(base, T * k);
   x->r.pos_tok = cv.take<int32_t>(base, P);
+  x->r.pos_w = cv.take<float>(base, P);
   x->r.act_e = cv.take<int32_t>(base, E + S);
   x->r.act_pos = cv.take<int32_t>(base, E + S);
   x->r.act_n = cv.take<int32_t>(base, E + S);
@@ -80,6 +81,9 @@ size_t carve(moe_ctx* x, uint8_t* base) {
   x->dbg_logits = cv.take<float>(base, T * E);
   x->h = cv.take<float>(base, P * f);
   x->yexp = cv.take<float>(base, P * d);
+  if (x->pf_enabled && prefill_accumulates(c, (int)T)) x->yacc = cv.take<float>(base, T * d);
+  else if (x->pf_enabled && prefill_accumulates(c, 1))
+    x->yacc = cv.take<float>(base, (size_t)(48u << 20) / (d * sizeof(float)) * d);
   x->status = cv.take<int>(base, 1);
   if (x->b1_enabled) {
     x->router_t = cv.take<float>(base, d * E);
@@ -418,7 +422,7 @@ moe_status moe_forward_prefill(moe_ctx* x, const void* x_bf16, int T, void* y_bf
   if (x->prof_start) CK(cudaEventRecordWithFlags(x->prof_start, s, cudaEventRecordExternal));
   CK(launch_prefill_experts(x, xb, T, s));
   if (x->prof_stop) CK(cudaEventRecordWithFlags(x->prof_stop, s, cudaEventRecordExternal));
-  CK(launch_combine(x, xb, T, static_cast<__nv_bfloat16*>(y_bf16), residual, s));
+  CK(launch_prefill_finish(x, xb, T, static_cast<__nv_bfloat16*>(y_bf16), residual, s));
   x->last_prefill_T = T;
   return MOE_OK;
 }
@@ -500,7 +504,7 @@ int moe_kernels_per_forward(moe_ctx* x, int T, int prefill) {
   if (!x || T <= 0) return 0;
   if (!prefill && T == 1 && x->b1_enabled) return 3;
   const int nb = bucket_kernel_count(T);
-  if (prefill) return 7 + nb;   // router x2, bucketing, quantise x, gather x, GEMM x2, combine
+  if (prefill) return 7 + nb;   // router x2, bucketing, quantise x, gather x, GEMM x2, finish
   if (x->mma_enabled) return 6 + nb;   // router x2, bucketing, x prescale, gate/up, down, combine
   return 5 + nb;
 }

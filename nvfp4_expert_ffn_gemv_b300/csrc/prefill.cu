@@ -20,8 +20,13 @@
 //              token, one TMEM lane) forms h = silu(g) * u for 64 hidden units
 //              in registers and quantises it to NVFP4 (block 16, scale 1):
 //              32 contiguous code bytes and 4 adjacent scale bytes per token;
-//   4. GEMM down: D[128 tokens, 128 output dims] * ts_down -> per-slot rows of
-//              yexp (fp32), then the decode path's fixed-order combine.
+//   4. GEMM down: D[128 tokens, 128 output dims] * ts_down * w is added with
+//              vector reductions into the token's row of an fp32 accumulator
+//              that stays in L2 (the weighted scatter-combine; the order of a
+//              token's seven contributions is not fixed), then one pass writes
+//              bf16 y (+ the residual).  Batches whose accumulator would not
+//              fit well inside L2 store per-position outputs instead and add
+//              them in a fixed order afterwards.
 //
 // GEMM kernel: persistent, one CTA (192 threads) per SM, 512 TMEM columns
 // (two 128-column accumulators, so the epilogue of one tile overlaps the MMAs
@@ -98,12 +103,17 @@ __device__ __forceinline__ size_t sf_atom_offset(int p, int b, int ksteps) {
   return ((size_t)(p >> 7) * ksteps + (b >> 2)) * 512 + (p & 31) * 16 + ((p >> 5) & 3) * 4 + (b & 3);
 }
 
-// x -> NVFP4, once per token (one warp per token, canonical layout).
+// x -> NVFP4, once per token (one warp per token, canonical layout); the
+// token's row of the fp32 output accumulator is cleared on the way.
 __global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int d,
-                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sc) {
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sc,
+                                                           float* __restrict__ yacc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
+  if (yacc)
+    for (int i = lane; i < d / 4; i += 32)
+      reinterpret_cast<float4*>(yacc + (size_t)t * d)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   const int nblk = d / 16;
   for (int b = lane; b < nblk; b += 32) {
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + b * 16);
@@ -167,13 +177,16 @@ struct GemmArgs {
   const float* tsc;       // [n_all][3]
   int M;                  // weight rows per expert (2f or d)
   int K;                  // contraction length
-  int mode;               // 0: gate/up -> h (NVFP4), 1: down -> yexp
+  int mode;               // 0: gate/up -> h (NVFP4), 1: down -> weighted adds into yacc
   // mode 0 outputs
   uint8_t* hq_codes;      // [rows][f/2]
   uint8_t* hq_sf;         // [rows/128][f/64][512]
   int f;
-  // mode 1 output
-  float* yexp;            // [positions][d]
+  // mode 1 output: with yacc, every position adds w * ts_down * D into its token's
+  // row of yacc (fp32 [T][d]); without, it stores ts_down * D into its own row of
+  // yexp (fp32 [positions][d]) for the fixed-order combine
+  float* yacc;
+  float* yexp;
   int d;
   int* status;
   int dbg;                // debug flags (MOE_DEBUG_FORCE_TIMEOUT)
@@ -395,20 +408,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // the 4 block scales of these 64 hidden units are one k-step of the down GEMM: 4 adjacent bytes
         if (ok) *reinterpret_cast<uint32_t*>(g.hq_sf + sf_atom_offset(p, ui.ntile * 4, g.f / 64)) = sc4;
       } else {
+        // weighted scatter-combine: w * ts_down * D is added into the token's
+        // row of the fp32 accumulator (vector reductions in L2; the order in
+        // which a token's top_k + shared contributions arrive is not fixed)
         const int i_tok = p - tab.ppos[ui.a];   // index among the expert's tokens
         const bool real = ok && m < ui.nt;
-        const float td = ts[2];
-        float* dst = g.yexp + (size_t)(tab.pos[ui.a] + i_tok) * g.d + ui.ntile * kBN;
+        const int pos = tab.pos[ui.a] + i_tok;
+        const bool acc = g.yacc != nullptr;
+        const int tok = (real && acc) ? __ldg(g.r.pos_tok + pos) : 0;
+        const float wtd = (real && acc) ? __ldg(g.r.pos_w + pos) * ts[2] : ts[2];
+        float* dst = acc ? g.yacc + (size_t)tok * g.d + ui.ntile * kBN : g.yexp + (size_t)pos * g.d + ui.ntile * kBN;
 #pragma unroll 1
         for (int c0 = 0; c0 < kBN; c0 += 32) {
           uint32_t v[32];
           if (ok) tmem_ld32(taddr + c0, v);
-          if (real) {
+          if (real && acc) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                           :: "l"(dst + c0 + j), "f"(__uint_as_float(v[j]) * wtd), "f"(__uint_as_float(v[j + 1]) * wtd),
+                              "f"(__uint_as_float(v[j + 2]) * wtd), "f"(__uint_as_float(v[j + 3]) * wtd)
+                           : "memory");
+          } else if (real) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
               *reinterpret_cast<float4*>(dst + c0 + j) =
-                  make_float4(__uint_as_float(v[j]) * td, __uint_as_float(v[j + 1]) * td,
-                              __uint_as_float(v[j + 2]) * td, __uint_as_float(v[j + 3]) * td);
+                  make_float4(__uint_as_float(v[j]) * wtd, __uint_as_float(v[j + 1]) * wtd,
+                              __uint_as_float(v[j + 2]) * wtd, __uint_as_float(v[j + 3]) * wtd);
           }
         }
       }
@@ -477,6 +503,11 @@ __global__ void weight_sf_atoms_kernel(const uint8_t* __restrict__ src, uint8_t*
 
 }  // namespace
 
+// The L2-resident accumulator pays while it stays well inside the 126 MB L2
+// next to the streamed weights (48 MB: 6144 tokens at d_model 2048); larger
+// batches store per-position outputs and combine them in a fixed order.
+bool prefill_accumulates(const moe_config& c, int T) { return (size_t)T * c.d_model * sizeof(float) <= (48u << 20); }
+
 bool prefill_supported(const moe_config& c) {
   return c.weight_format == MOE_W_NVFP4 && c.d_model % 256 == 0 && c.d_ff % 256 == 0 && c.d_model <= 8192;
 }
@@ -506,7 +537,8 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   const int d = c->cfg.d_model, f = c->cfg.d_ff;
   const int rows = (int)prefill_max_rows(c->cfg);
   cudaError_t e;
-  quant_tokens_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, d, c->pf_xq_tok, c->pf_xsf_tok);
+  quant_tokens_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, d, c->pf_xq_tok, c->pf_xsf_tok,
+                                                  prefill_accumulates(c->cfg, T) ? c->yacc : nullptr);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gather_x_kernel<<<(rows + 7) / 8, 256, 0, s>>>(c->r, c->pf_xq_tok, c->pf_xsf_tok, d, c->pf_xq, c->pf_xsf, rows);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -533,8 +565,37 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   g.M = d;
   g.K = f;
   g.mode = 1;
+  g.yacc = prefill_accumulates(c->cfg, T) ? c->yacc : nullptr;
   g.yexp = c->yexp;
   moe_gemm_kernel<<<c->sm_count, kGemmThreads, kSmemGemm, s>>>(c->pf_tm[3], c->pf_tm[1], g);
+  return cudaGetLastError();
+}
+
+// y = bf16(yacc (+ x)), four elements per thread
+namespace {
+__global__ void __launch_bounds__(256) prefill_finish_kernel(const float* __restrict__ yacc,
+                                                             const __nv_bfloat16* __restrict__ x, size_t n4,
+                                                             int residual, __nv_bfloat16* __restrict__ y) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  float4 a = reinterpret_cast<const float4*>(yacc)[i];
+  if (residual) {
+    const uint2 xv = reinterpret_cast<const uint2*>(x)[i];
+    a.x += __uint_as_float(xv.x << 16);
+    a.y += __uint_as_float(xv.x & 0xFFFF0000u);
+    a.z += __uint_as_float(xv.y << 16);
+    a.w += __uint_as_float(xv.y & 0xFFFF0000u);
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+  reinterpret_cast<uint2*>(y)[i] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+}
+}  // namespace
+
+cudaError_t launch_prefill_finish(const moe_ctx* c, const __nv_bfloat16* x, int T, __nv_bfloat16* y, int residual,
+                                  cudaStream_t s) {
+  if (!prefill_accumulates(c->cfg, T)) return launch_combine(c, x, T, y, residual, s);
+  const size_t n4 = (size_t)T * c->cfg.d_model / 4;
+  prefill_finish_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(c->yacc, x, n4, residual, y);
   return cudaGetLastError();
 }
 

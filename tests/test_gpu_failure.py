@@ -9,7 +9,9 @@
   MOE_DEBUG_FORCE_TIMEOUT makes the batch-1 decode kernels, the prefill GEMMs
   and the tensor-core router report a timeout after their real waits have
   completed (no copy or MMA is left in flight); the status is reported once,
-  and the output is the same as without the flag.  Batched decode (T >= 2)
+  and the output is the same as without the flag (bit for bit on the batch-1
+  path; prefill adds a token's expert contributions in arrival order, so
+  there it agrees to rounding).  Batched decode (T >= 2)
   has no device-side waits.
 * Allocation failure: moe_debug_fail_alloc makes the n-th device allocation
   of the library fail -- the arena of moe_init, or (n = 2 on a batch-1
@@ -86,8 +88,13 @@ def test_forced_timeout_reaches_status_word(lib, path):
         lib.moe_set_debug(layer.ctx, 0)
         again = run(lib, layer, xb, T)
         assert lib.moe_get_device_status(layer.ctx) == 0
-        assert torch.equal(clean.view(torch.int16), forced.view(torch.int16))
-        assert torch.equal(clean.view(torch.int16), again.view(torch.int16))
+        if path == "batch1":     # fixed summation order: bit-identical
+            assert torch.equal(clean.view(torch.int16), forced.view(torch.int16))
+            assert torch.equal(clean.view(torch.int16), again.view(torch.int16))
+        else:                    # prefill adds a token's contributions in arrival order
+            for other in (forced, again):
+                rel, mx = harness.compare(other, clean.float().cpu().numpy())
+                assert rel <= 1e-4 and mx <= 1e-2, (rel, mx)
     finally:
         lib.moe_destroy(layer.ctx)
 
