@@ -64,8 +64,6 @@ struct moe_ctx {
   int last_prefill_T = -1;
   uint8_t* pf_sfa_gu = nullptr;  // gate/up weight scale atoms [n_all][2f/128][d/64][512]
   uint8_t* pf_sfa_dn = nullptr;  // W_down scale atoms [n_all][d/128][f/64][512]
-  uint8_t* pf_xq_tok = nullptr;  // x in NVFP4 per token [max_tokens][d/2]
-  uint8_t* pf_xsf_tok = nullptr; // its E4M3 block scales [max_tokens][d/16]
   uint8_t* pf_xq = nullptr;      // x in NVFP4, padded positions [rows][d/2]
   uint8_t* pf_xsf = nullptr;     // its scale atoms [rows/128][d/64][512]
   uint8_t* pf_hq = nullptr;      // h in NVFP4 [rows][f/2]

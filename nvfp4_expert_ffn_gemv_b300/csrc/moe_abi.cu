@@ -103,8 +103,6 @@ size_t carve(moe_ctx* x, uint8_t* base) {
     const size_t rows = prefill_max_rows(c);
     x->pf_sfa_gu = cv.take<uint8_t>(base, n * 2 * f * d / 16);
     x->pf_sfa_dn = cv.take<uint8_t>(base, n * d * f / 16);
-    x->pf_xq_tok = cv.take<uint8_t>(base, T * d / 2);
-    x->pf_xsf_tok = cv.take<uint8_t>(base, T * d / 16);
     x->pf_xq = cv.take<uint8_t>(base, rows * d / 2);
     x->pf_xsf = cv.take<uint8_t>(base, rows * d / 16);
     x->pf_hq = cv.take<uint8_t>(base, rows * f / 2);

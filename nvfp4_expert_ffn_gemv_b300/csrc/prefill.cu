@@ -28,14 +28,20 @@
 //              fit well inside L2 store per-position outputs instead and add
 //              them in a fixed order afterwards.
 //
-// GEMM kernel: persistent, one CTA (192 threads) per SM, 512 TMEM columns
+// GEMM kernel: persistent, one CTA (320 threads) per SM, 512 TMEM columns
 // (two 128-column accumulators, so the epilogue of one tile overlaps the MMAs
-// of the next, plus 4 stages x 32 scale-factor columns).
-//   warp 0  TMA producer: 4-stage ring of {A 128x256 fp4 tokens (SW128),
-//           B 128x256 fp4 weights (SW128), SFA 4 atoms, SFB 4 atoms}
+// of the next, plus 32 scale-factor columns per stage).
+//   warp 0  TMA producer: ring of {A 128x256 fp4 tokens (SW128),
+//           B 128x256 fp4 weights (SW128), SFA 4 atoms, SFB 4 atoms}, 6 stages
+//           in the gate/up GEMM, 4 in the down GEMM (whose epilogue needs
+//           shared memory too)
 //   warp 1  TMEM owner + single-thread MMA issuer: per stage, scale atoms ->
 //           TMEM (tcgen05.cp 32x128b.warpx4), 4 MMAs of K = 64
-//   warps 2-5 epilogue (TMEM lanes 32*(warp%4) ..), tcgen05.ld 32 columns
+//   warps 2-9 epilogue: two warps per TMEM lane quarter (lanes 32*(warp%4) ..),
+//           each taking half of the tile's columns (tcgen05.ld 32 at a time).
+//           The down GEMM's rows go through a per-warp shared-memory tile so
+//           that each vector reduction covers 4 rows x 128 contiguous bytes
+//           instead of 32 scattered rows (2x the reduction rate into L2).
 // All waits are bounded; the first one that gives up latches MOE_ERR_TIMEOUT
 // and sets a CTA-wide abort flag so that no other role waits afterwards.
 #include <cuda.h>
@@ -53,22 +59,39 @@ using namespace sm100;
 constexpr int kBM = 128;        // tokens per tile (MMA M, TMEM lanes)
 constexpr int kBN = 128;        // weight rows per tile (MMA N)
 constexpr int kStageK = 256;    // fp4 elements of K per stage (128 bytes per row)
-constexpr int kStages = 4;
-constexpr int kGemmThreads = 192;
+constexpr int kStagesGateUp = 6;   // gate/up: 6 x 36 KB in flight (no epilogue staging)
+constexpr int kStagesDown = 4;     // down: 4 x 36 KB + the epilogue's row staging
+constexpr int kEpiWarps = 8;
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSfCol0 = 2 * kBN;      // scale-factor columns after the two accumulators
-constexpr int kSfColsPerStage = 32;   // SFA 4 k-steps x 4 + SFB 4 k-steps x 4
+// TMEM columns: two 128-column accumulators, then a ring of token-side scales
+// (SFA) and one of weight-side scales (SFB), 16 columns per stage each (a
+// k-step of 64 values of K takes 4 columns of scales per operand).
+constexpr int kSfaCol0 = 2 * kBN;
+constexpr int kSfbCol0 = kSfaCol0 + 128;
+constexpr int kSfColsPerStage = 16;
 
 // shared-memory plan of the GEMM kernel (offsets from a 1024-aligned base)
 constexpr int kA = kBM * 128;                 // 16 KB per stage
 constexpr int kB = kBN * 128;                 // 16 KB per stage
 constexpr int kSF = 4 * 512;                  // 2 KB per operand per stage
 constexpr int kStageBytes = kA + kB + 2 * kSF;
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kA;
-constexpr int kOffSFA = kOffB + kStages * kB;
-constexpr int kOffSFB = kOffSFA + kStages * kSF;
-constexpr int kSmemGemm = kOffSFB + kStages * kSF + 1024;  // + alignment slack
+constexpr int kEpiStride = 144;             // staged row: 32 fp32 + 16 bytes of padding (no bank conflicts)
+constexpr int kEpiBytes = kEpiWarps * 32 * kEpiStride;
+// ring of NST stages {A, B, SFA, SFB} from a 1024-aligned base, then (down
+// GEMM only) the epilogue's staging rows
+template <int NST>
+struct Plan {
+  static constexpr int offA = 0;
+  static constexpr int offB = offA + NST * kA;
+  static constexpr int offSFA = offB + NST * kB;
+  static constexpr int offSFB = offSFA + NST * kSF;
+  static constexpr int offEpi = offSFB + NST * kSF;
+  static_assert(kSfbCol0 + NST * kSfColsPerStage <= (int)kTmemCols, "scale-factor columns exceed TMEM");
+  static_assert(NST * kSfColsPerStage <= kSfbCol0 - kSfaCol0, "SFA ring overlaps SFB");
+};
+constexpr int kSmemGateUp = Plan<kStagesGateUp>::offEpi + 1024;               // + alignment slack
+constexpr int kSmemDown = Plan<kStagesDown>::offEpi + kEpiBytes + 1024;
 
 // largest a < na with tab[a] <= v (tab non-decreasing, tab[0] = 0)
 __device__ __forceinline__ int find_seg(const int32_t* tab, int na, int v) {
@@ -88,14 +111,15 @@ __device__ __forceinline__ uint32_t q_e4m3(float v) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(0.0f), "f"(v));
   return out & 0xFF;
 }
-__device__ __forceinline__ uint32_t q_e2m1x2(float even, float odd) {
-  uint16_t out;
-  asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n\tcvt.u16.u8 %0, b;\n\t}"
-      : "=h"(out) : "f"(odd), "f"(even));
-  uint32_t v = out & 0xFF;
-  if ((v & 0x07) == 0) v &= 0xF0;
-  if ((v & 0x70) == 0) v &= 0x0F;
-  return v;
+// E2M1 code of v / dq, rounded to nearest with ties to the even code, decided
+// without dividing: |v| is compared with each rounding midpoint times dq.
+// Midpoints have at most 3 significant bits and dq (an E4M3 value) at most 4,
+// so every product is exact and the comparison is that of the exact quotient.
+__device__ __forceinline__ uint32_t e2m1_by_compare(float v, float dq) {
+  const float a = fabsf(v);
+  const uint32_t c = (a > 0.25f * dq) + (a >= 0.75f * dq) + (a > 1.25f * dq) + (a >= 1.75f * dq) +
+                     (a > 2.5f * dq) + (a >= 3.5f * dq) + (a > 5.0f * dq);
+  return (v < 0.f && c != 0u) ? (c | 8u) : c;
 }
 
 // byte offset of the scale of (row p, 16-block b) in a [rows/128][ksteps][512] atom array
@@ -103,68 +127,99 @@ __device__ __forceinline__ size_t sf_atom_offset(int p, int b, int ksteps) {
   return ((size_t)(p >> 7) * ksteps + (b >> 2)) * 512 + (p & 31) * 16 + ((p >> 5) & 3) * 4 + (b & 3);
 }
 
-// x -> NVFP4, once per token (one warp per token, canonical layout); the
-// token's row of the fp32 output accumulator is cleared on the way.
-__global__ void __launch_bounds__(256) quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int d,
-                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sc,
-                                                           float* __restrict__ yacc) {
+// Active-expert tables copied to shared memory once per CTA, so that mapping a
+// tile index to its expert costs shared-memory reads only (a binary search
+// over global memory would put several dependent L2 round trips in front of
+// every TMA issue).
+constexpr int kMaxActive = 256 + 2 + 1;
+struct ActTables {
+  int ppos[kMaxActive];   // padded first row, total last
+  int e[kMaxActive];
+  int n[kMaxActive];
+  int pos[kMaxActive];
+};
+
+// x -> NVFP4 (tensor scale 1), once per token, written straight into the
+// token's k + S padded rows of the grouped-GEMM operand (codes) and into the
+// MMA's scale-factor atoms (scales).  One warp per token; each lane quantises
+// four consecutive 16-element blocks (one k-step) at a time.  The token's row
+// of the fp32 output accumulator is cleared on the way.  Padding rows of the
+// position blocks are not written: the GEMM rows are independent and the
+// outputs of padding rows are never read.
+constexpr int kMaxPerTok = 10;   // top_k (<= 8) + n_shared (<= 2)
+__global__ void __launch_bounds__(256, 3) quant_scatter_x_kernel(Routing r, const __nv_bfloat16* __restrict__ x, int T,
+                                                              int d, int k, int S, uint8_t* __restrict__ codes,
+                                                              uint8_t* __restrict__ sf, float* __restrict__ yacc) {
+  __shared__ int s_pos[kMaxActive], s_ppos[kMaxActive], s_prow[8][kMaxPerTok];
+  const int na = *r.n_active;
+  for (int i = threadIdx.x; i <= na; i += blockDim.x) {
+    s_pos[i] = i < na ? r.act_pos[i] : 0;
+    s_ppos[i] = r.act_ppos[i];
+  }
+  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
+  // lane j < k + S finds the padded row of the token's j-th position
+  if (lane < k + S) {
+    const int pos = lane < k ? __ldg(r.slot_pos + (size_t)t * k + lane) : T * k + (lane - k) * T + t;
+    int lo = 0, hi = na - 1;               // last active expert whose first position is <= pos
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pos[mid] <= pos) lo = mid; else hi = mid - 1;
+    }
+    s_prow[warp][lane] = s_ppos[lo] + (pos - s_pos[lo]);
+  }
+  __syncwarp();
+  const int* pr = s_prow[warp];
   if (yacc)
     for (int i = lane; i < d / 4; i += 32)
       reinterpret_cast<float4*>(yacc + (size_t)t * d)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int nblk = d / 16;
-  for (int b = lane; b < nblk; b += 32) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + b * 16);
-    const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-    float v[16];
+  const int nblk = d / 16, ksteps = d / 64;
+  for (int b0 = 4 * lane; b0 < nblk; b0 += 128) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + b0 * 16);
+    uint4 u[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      v[2 * q] = __uint_as_float(w[q] << 16);
-      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
-    }
-    float amax = 0.f;
+    for (int q = 0; q < 8; ++q) u[q] = __ldg(src + q);
+    uint32_t cw[8], sc = 0;
 #pragma unroll
-    for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
-    const uint32_t s = q_e4m3(__fdiv_rn(amax, 6.0f));
-    const float dq = e4m3_to_f32(s);
-    uint32_t lo = 0, hi = 0;
-    if (dq > 0.f) {
+    for (int blk = 0; blk < 4; ++blk) {
+      const uint32_t w[8] = {u[2 * blk].x, u[2 * blk].y, u[2 * blk].z, u[2 * blk].w,
+                             u[2 * blk + 1].x, u[2 * blk + 1].y, u[2 * blk + 1].z, u[2 * blk + 1].w};
+      float v[16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        lo |= q_e2m1x2(__fdiv_rn(v[2 * q], dq), __fdiv_rn(v[2 * q + 1], dq)) << (8 * q);
-        hi |= q_e2m1x2(__fdiv_rn(v[8 + 2 * q], dq), __fdiv_rn(v[8 + 2 * q + 1], dq)) << (8 * q);
+      for (int q = 0; q < 8; ++q) {
+        v[2 * q] = __uint_as_float(w[q] << 16);
+        v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
       }
+      float amax = 0.f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+      const uint32_t s8 = q_e4m3(__fdiv_rn(amax, 6.0f));
+      const float dq = e4m3_to_f32(s8);
+      uint32_t lo = 0, hi = 0;
+      // codes by comparison with midpoint x dq (exact products).  For a bf16
+      // value this equals rounding the fp32 quotient v / dq: the exact quotient
+      // is a midpoint itself or at least ~2^-8 (relative) away from every midpoint.
+      if (dq > 0.f) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          lo |= e2m1_by_compare(v[q], dq) << (4 * q);
+          hi |= e2m1_by_compare(v[8 + q], dq) << (4 * q);
+        }
+      }
+      cw[2 * blk] = lo;
+      cw[2 * blk + 1] = hi;
+      sc |= s8 << (8 * blk);
     }
-    reinterpret_cast<uint2*>(codes + (size_t)t * (d / 2))[b] = make_uint2(lo, hi);
-    sc[(size_t)t * nblk + b] = static_cast<uint8_t>(s);
+    for (int j = 0; j < k + S; ++j) {
+      const int p = pr[j];
+      uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)p * (d / 2) + b0 * 8);
+      dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+      *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(p, b0, ksteps)) = sc;   // blocks b0..b0+3: one k-step
+    }
   }
-}
-
-// Quantised token rows -> padded position order, scales into the MMA's
-// scale-factor atoms (one warp per padded row; padding rows are zero).
-__global__ void __launch_bounds__(256) gather_x_kernel(Routing r, const uint8_t* __restrict__ tq,
-                                                       const uint8_t* __restrict__ tsc, int d,
-                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-                                                       int max_rows) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = blockIdx.x * 8 + warp;
-  const int na = *r.n_active;
-  const int total = r.act_ppos[na];
-  if (p >= total || p >= max_rows) return;
-  const int a = r.blk_a[p >> 7];
-  const int i = p - r.act_ppos[a];
-  const bool real = i < r.act_n[a];
-  const int t = real ? r.pos_tok[r.act_pos[a] + i] : 0;
-  const int ksteps = d / 64;
-  const uint4* src = reinterpret_cast<const uint4*>(tq + (size_t)t * (d / 2));
-  uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)p * (d / 2));
-  for (int q = lane; q < d / 32; q += 32) dst[q] = real ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
-  const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(tsc + (size_t)t * (d / 16));
-  for (int ks = lane; ks < ksteps; ks += 32)
-    *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(p, 4 * ks, ksteps)) = real ? __ldg(ssrc + ks) : 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -177,7 +232,6 @@ struct GemmArgs {
   const float* tsc;       // [n_all][3]
   int M;                  // weight rows per expert (2f or d)
   int K;                  // contraction length
-  int mode;               // 0: gate/up -> h (NVFP4), 1: down -> weighted adds into yacc
   // mode 0 outputs
   uint8_t* hq_codes;      // [rows][f/2]
   uint8_t* hq_sf;         // [rows/128][f/64][512]
@@ -190,18 +244,6 @@ struct GemmArgs {
   int d;
   int* status;
   int dbg;                // debug flags (MOE_DEBUG_FORCE_TIMEOUT)
-};
-
-// Active-expert tables copied to shared memory once per CTA, so that mapping a
-// tile index to its expert costs shared-memory reads only (a binary search
-// over global memory would put several dependent L2 round trips in front of
-// every TMA issue).
-constexpr int kMaxActive = 256 + 2 + 1;
-struct ActTables {
-  int ppos[kMaxActive];   // padded first row, total last
-  int e[kMaxActive];
-  int n[kMaxActive];
-  int pos[kMaxActive];
 };
 
 // unit u -> (128-token block, 128-row weight tile)
@@ -227,17 +269,6 @@ __device__ __forceinline__ UnitInfo decode_unit(const ActTables& t, int u, int n
 
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
-// E2M1 code of v / dq, rounded to nearest with ties to the even code, decided
-// without dividing: |v| is compared with each rounding midpoint times dq.
-// Midpoints have at most 3 significant bits and dq (an E4M3 value) at most 4,
-// so every product is exact and the comparison is that of the exact quotient.
-__device__ __forceinline__ uint32_t e2m1_by_compare(float v, float dq) {
-  const float a = fabsf(v);
-  const uint32_t c = (a > 0.25f * dq) + (a >= 0.75f * dq) + (a > 1.25f * dq) + (a >= 1.75f * dq) +
-                     (a > 2.5f * dq) + (a >= 3.5f * dq) + (a > 5.0f * dq);
-  return (v < 0.f && c != 0u) ? (c | 8u) : c;
-}
-
 // NVFP4 (scale 1) of 16 consecutive fp32 values held by one thread -> 8 code bytes, one scale byte
 __device__ __forceinline__ uint32_t quant16(const float* v, uint2& codes) {
   float amax = 0.f;
@@ -257,11 +288,13 @@ __device__ __forceinline__ uint32_t quant16(const float* v, uint2& codes) {
   return s;
 }
 
+template <int NST, int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
+  using P = Plan<NST>;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], dfull_bar[2], dempty_bar[2];
+  __shared__ __align__(8) uint64_t full_bar[NST], empty_bar[NST], dfull_bar[2], dempty_bar[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_flag;
   __shared__ ActTables tab;
@@ -278,13 +311,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int ntiles = g.M / kBN, ksteps = g.K / 64, kstages = g.K / kStageK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&dfull_bar[b], 1);
-      mbar_init(&dempty_bar[b], 4);
+      mbar_init(&dempty_bar[b], kEpiWarps);
     }
     abort_flag = 0;
     fence_barrier_init();
@@ -299,6 +332,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   const int U = (tab.ppos[na] / kBM) * ntiles;
+
 
   auto bounded_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (abort_flag) return false;
@@ -321,11 +355,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int ks = 0; ks < kstages; ++ks) {
           if (!bounded_wait(&empty_bar[stage], phase ^ 1)) break;
           mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
-          tma_load_2d(smem + kOffA + stage * kA, &tmA, ks * 128, ui.p0, &full_bar[stage]);
-          tma_load_2d(smem + kOffB + stage * kB, &tmB, ks * 128, brow, &full_bar[stage]);
-          bulk_load(smem + kOffSFA + stage * kSF, sfa + (size_t)ks * 4 * 512, kSF, &full_bar[stage]);
-          bulk_load(smem + kOffSFB + stage * kSF, sfb + (size_t)ks * 4 * 512, kSF, &full_bar[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          tma_load_2d(smem + P::offA + stage * kA, &tmA, ks * 128, ui.p0, &full_bar[stage]);
+          tma_load_2d(smem + P::offB + stage * kB, &tmB, ks * 128, brow, &full_bar[stage]);
+          bulk_load(smem + P::offSFA + stage * kSF, sfa + (size_t)ks * 4 * 512, kSF, &full_bar[stage]);
+          bulk_load(smem + P::offSFB + stage * kSF, sfb + (size_t)ks * 4 * 512, kSF, &full_bar[stage]);
+          if (++stage == NST) { stage = 0; phase ^= 1; }
         }
       }
     }
@@ -344,34 +378,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int ks = 0; ks < kstages; ++ks) {
           if (!bounded_wait(&full_bar[stage], phase)) break;
           tc_fence_after();
-          const uint32_t sf = tmem + kSfCol0 + stage * kSfColsPerStage;
-          const uint32_t sa = smem_u32(smem + kOffSFA + stage * kSF);
-          const uint32_t sb = smem_u32(smem + kOffSFB + stage * kSF);
+          const uint32_t sfa_t = tmem + kSfaCol0 + stage * kSfColsPerStage;
+          const uint32_t sfb_t = tmem + kSfbCol0 + stage * kSfColsPerStage;
+          const uint32_t sa = smem_u32(smem + P::offSFA + stage * kSF);
+          const uint32_t sb = smem_u32(smem + P::offSFB + stage * kSF);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            tmem_cp_sf_atom(sf + kk * 4, desc_sf_atom(sa + kk * 512));
-            tmem_cp_sf_atom(sf + 16 + kk * 4, desc_sf_atom(sb + kk * 512));
+            tmem_cp_sf_atom(sfa_t + kk * 4, desc_sf_atom(sa + kk * 512));
+            tmem_cp_sf_atom(sfb_t + kk * 4, desc_sf_atom(sb + kk * 512));
           }
-          const uint64_t adesc = desc_kmajor_sw128(smem_u32(smem + kOffA + stage * kA));
-          const uint64_t bdesc = desc_kmajor_sw128(smem_u32(smem + kOffB + stage * kB));
+          const uint64_t adesc = desc_kmajor_sw128(smem_u32(smem + P::offA + stage * kA));
+          const uint64_t bdesc = desc_kmajor_sw128(smem_u32(smem + P::offB + stage * kB));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_mxf4nvf4(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, sf + kk * 4,
-                         sf + 16 + kk * 4, ks > 0 || kk > 0);
+            mma_mxf4nvf4(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, sfa_t + kk * 4,
+                         sfb_t + kk * 4, ks > 0 || kk > 0);
           tc_commit(&empty_bar[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (++stage == NST) { stage = 0; phase ^= 1; }
         }
         tc_commit(&dfull_bar[buf]);
       }
     }
   } else {
     // ------------------------------ epilogue ------------------------------
-    // TMEM lane = token row of the block; this thread owns token row m.
-    const int q = warp & 3;
+    // TMEM lane = token row of the block; this thread owns token row m and
+    // column half hsel of the tile.
+    const int q = warp & 3, hsel = (warp - 2) >> 2;
     const int m = q * 32 + lane;
+    uint8_t* stage_rows = smem + P::offEpi + (warp - 2) * 32 * kEpiStride;
     int i = 0;
     // Every epilogue warp runs the same units and never leaves the loop early
-    // (a failed wait only skips the work), so all four always arrive.
+    // (a failed wait only skips the work), so all of them always arrive.
     for (int u = blockIdx.x; u < U; u += gridDim.x, ++i) {
       const UnitInfo ui = decode_unit(tab, u, ntiles, na);
       const int buf = i & 1;
@@ -380,61 +417,70 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * kBN;
       const float* ts = g.tsc + ui.e * 3;
       const int p = ui.p0 + m;                    // padded row of this token
-      if (g.mode == 0) {
-        // columns 0..63 gate rows, 64..127 up rows of hidden units 64*ntile + 0..63
+      if constexpr (MODE == 0) {
+        // columns 0..63 gate rows, 64..127 up rows of hidden units 64*ntile + 0..63;
+        // this warp forms hidden units 32*hsel .. 32*hsel+31
         const float tg = ts[0], tu = ts[1];
-        uint32_t sc4 = 0;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t gv[32], uv[32];
-          if (ok) {
-            tmem_ld32(taddr + half * 32, gv);
-            tmem_ld32(taddr + 64 + half * 32, uv);
-          } else {
+        uint32_t gv[32], uv[32];
+        if (ok) {
+          tmem_ld32(taddr + hsel * 32, gv);
+          tmem_ld32(taddr + 64 + hsel * 32, uv);
+        } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) { gv[j] = 0u; uv[j] = 0u; }
-          }
-          float hv[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            hv[j] = silu_fast(__uint_as_float(gv[j]) * tg) * (__uint_as_float(uv[j]) * tu);
-          uint2 c0, c1;
-          const uint32_t s0 = quant16(hv, c0), s1 = quant16(hv + 16, c1);
-          sc4 |= (s0 | (s1 << 8)) << (16 * half);
-          if (ok)
-            *reinterpret_cast<uint4*>(g.hq_codes + (size_t)p * (g.f / 2) + ui.ntile * 32 + half * 16) =
-                make_uint4(c0.x, c0.y, c1.x, c1.y);
+          for (int j = 0; j < 32; ++j) { gv[j] = 0u; uv[j] = 0u; }
         }
-        // the 4 block scales of these 64 hidden units are one k-step of the down GEMM: 4 adjacent bytes
-        if (ok) *reinterpret_cast<uint32_t*>(g.hq_sf + sf_atom_offset(p, ui.ntile * 4, g.f / 64)) = sc4;
-      } else {
+        float hv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          hv[j] = silu_fast(__uint_as_float(gv[j]) * tg) * (__uint_as_float(uv[j]) * tu);
+        uint2 c0, c1;
+        const uint32_t s0 = quant16(hv, c0), s1 = quant16(hv + 16, c1);
+        if (ok) {
+          *reinterpret_cast<uint4*>(g.hq_codes + (size_t)p * (g.f / 2) + ui.ntile * 32 + hsel * 16) =
+              make_uint4(c0.x, c0.y, c1.x, c1.y);
+          // the 4 block scales of these 64 hidden units are one k-step of the
+          // down GEMM (4 adjacent bytes); this warp writes two of them
+          *reinterpret_cast<uint16_t*>(g.hq_sf + sf_atom_offset(p, ui.ntile * 4, g.f / 64) + 2 * hsel) =
+              static_cast<uint16_t>(s0 | (s1 << 8));
+        }
+      } else if (ok) {
         // weighted scatter-combine: w * ts_down * D is added into the token's
         // row of the fp32 accumulator (vector reductions in L2; the order in
-        // which a token's top_k + shared contributions arrive is not fixed)
+        // which a token's top_k + shared contributions arrive is not fixed).
+        // Without the accumulator, ts_down * D goes to the position's own row.
         const int i_tok = p - tab.ppos[ui.a];   // index among the expert's tokens
-        const bool real = ok && m < ui.nt;
+        const bool real = m < ui.nt;
         const int pos = tab.pos[ui.a] + i_tok;
         const bool acc = g.yacc != nullptr;
-        const int tok = (real && acc) ? __ldg(g.r.pos_tok + pos) : 0;
+        const int row_out = !real ? 0 : acc ? __ldg(g.r.pos_tok + pos) : pos;
         const float wtd = (real && acc) ? __ldg(g.r.pos_w + pos) * ts[2] : ts[2];
-        float* dst = acc ? g.yacc + (size_t)tok * g.d + ui.ntile * kBN : g.yexp + (size_t)pos * g.d + ui.ntile * kBN;
+        const unsigned real_mask = __ballot_sync(0xffffffffu, real);
+        float* base = (acc ? g.yacc : g.yexp) + ui.ntile * kBN;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
+        for (int c0 = hsel * 64; c0 < hsel * 64 + 64; c0 += 32) {
           uint32_t v[32];
-          if (ok) tmem_ld32(taddr + c0, v);
-          if (real && acc) {
+          tmem_ld32(taddr + c0, v);
+          __syncwarp();                         // the previous chunk's rows have been read
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-                           :: "l"(dst + c0 + j), "f"(__uint_as_float(v[j]) * wtd), "f"(__uint_as_float(v[j + 1]) * wtd),
-                              "f"(__uint_as_float(v[j + 2]) * wtd), "f"(__uint_as_float(v[j + 3]) * wtd)
-                           : "memory");
-          } else if (real) {
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(stage_rows + lane * kEpiStride + j * 4) =
+                make_float4(__uint_as_float(v[j]) * wtd, __uint_as_float(v[j + 1]) * wtd,
+                            __uint_as_float(v[j + 2]) * wtd, __uint_as_float(v[j + 3]) * wtd);
+          __syncwarp();
+          // 8 lanes per row: each instruction covers 4 rows x 128 contiguous bytes
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4*>(dst + c0 + j) =
-                  make_float4(__uint_as_float(v[j]) * wtd, __uint_as_float(v[j + 1]) * wtd,
-                              __uint_as_float(v[j + 2]) * wtd, __uint_as_float(v[j + 3]) * wtd);
+          for (int rr = 0; rr < 32; rr += 4) {
+            const int row = rr + (lane >> 3), qq = lane & 7;
+            const int dst_row = __shfl_sync(0xffffffffu, row_out, row);
+            if ((real_mask >> row) & 1u) {
+              const float4 x = *reinterpret_cast<const float4*>(stage_rows + row * kEpiStride + qq * 16);
+              float* dst = base + (size_t)dst_row * g.d + c0 + qq * 4;
+              if (acc)
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                             :: "l"(dst), "f"(x.x), "f"(x.y), "f"(x.z), "f"(x.w) : "memory");
+              else
+                *reinterpret_cast<float4*>(dst) = x;
+            }
           }
         }
       }
@@ -530,17 +576,18 @@ cudaError_t prefill_prepare(moe_ctx* c) {
             make_tmap(&c->pf_tm[2], c->pf_xq, rows, d / 2, kBM) &&
             make_tmap(&c->pf_tm[3], c->pf_hq, rows, f / 2, kBM);
   if (!ok) return cudaErrorInvalidValue;
-  return cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGemm);
+  e = cudaFuncSetAttribute(moe_gemm_kernel<kStagesGateUp, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemGateUp);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(moe_gemm_kernel<kStagesDown, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemDown);
 }
 
 cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s) {
   const int d = c->cfg.d_model, f = c->cfg.d_ff;
-  const int rows = (int)prefill_max_rows(c->cfg);
   cudaError_t e;
-  quant_tokens_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, d, c->pf_xq_tok, c->pf_xsf_tok,
-                                                  prefill_accumulates(c->cfg, T) ? c->yacc : nullptr);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  gather_x_kernel<<<(rows + 7) / 8, 256, 0, s>>>(c->r, c->pf_xq_tok, c->pf_xsf_tok, d, c->pf_xq, c->pf_xsf, rows);
+  quant_scatter_x_kernel<<<(T + 7) / 8, 256, 0, s>>>(c->r, x, T, d, c->cfg.top_k, c->cfg.n_shared, c->pf_xq,
+                                                     c->pf_xsf, prefill_accumulates(c->cfg, T) ? c->yacc : nullptr);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   GemmArgs g{};
   g.r = c->r;
@@ -554,20 +601,18 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   g.sfb = c->pf_sfa_gu;
   g.M = 2 * f;
   g.K = d;
-  g.mode = 0;
   g.hq_codes = c->pf_hq;
   g.hq_sf = c->pf_hsf;
-  moe_gemm_kernel<<<c->sm_count, kGemmThreads, kSmemGemm, s>>>(c->pf_tm[2], c->pf_tm[0], g);
+  moe_gemm_kernel<kStagesGateUp, 0><<<c->sm_count, kGemmThreads, kSmemGateUp, s>>>(c->pf_tm[2], c->pf_tm[0], g);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // down projection -> per-slot outputs
   g.sfa = c->pf_hsf;
   g.sfb = c->pf_sfa_dn;
   g.M = d;
   g.K = f;
-  g.mode = 1;
   g.yacc = prefill_accumulates(c->cfg, T) ? c->yacc : nullptr;
   g.yexp = c->yexp;
-  moe_gemm_kernel<<<c->sm_count, kGemmThreads, kSmemGemm, s>>>(c->pf_tm[3], c->pf_tm[1], g);
+  moe_gemm_kernel<kStagesDown, 1><<<c->sm_count, kGemmThreads, kSmemDown, s>>>(c->pf_tm[3], c->pf_tm[1], g);
   return cudaGetLastError();
 }
 

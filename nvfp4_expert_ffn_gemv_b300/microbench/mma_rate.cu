@@ -1,0 +1,115 @@
+// Issue rate of the block-scaled FP4 tensor-core path on one SM: how long a
+// K = 256 stage of tcgen05.mma kind::mxf4nvf4 (4 MMAs of K = 64) and its
+// scale-factor copies (tcgen05.cp 32x128b.warpx4, one per 512-byte atom) take
+// when issued back to back by one thread, operands resident in shared memory.
+//   mma N=128 / N=256      4 MMAs per stage, M = 128
+//   cp x8                  the 8 scale-factor copies of a 128 x 128 stage alone
+//   cp x8 + mma N=128      the prefill GEMM's stage (A and B scales per k-step)
+//   cp x12 + mma N=256     a 128 x 256 stage (B scales for 256 rows)
+//   cp x4 + mma N=128      B scales only (A scales kept in TMEM)
+//   cp x8 + mma N=256      B scales only, 128 x 256
+// Every CTA (one per SM) runs 256 stages; the time is from the first issue to
+// the completion of the last operation (tcgen05.commit), in SM cycles.
+// Operand values are arbitrary: only the rate is measured.
+#include <cstdio>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../csrc/sm100.cuh"
+
+using namespace nvmoe::sm100;
+
+#define CK(x) do { cudaError_t err_ = (x); if (err_ != cudaSuccess) { \
+  printf("CUDA error %s at %s:%d\n", cudaGetErrorString(err_), __FILE__, __LINE__); return 1; } } while (0)
+
+constexpr int kStages = 256;
+constexpr int kOffA = 0, kOffB = 16384, kOffSF = 49152, kUsed = kOffSF + 12 * 512;
+constexpr int kSmem = 120 * 1024;   // more than half an SM's shared memory: one CTA per SM
+
+struct Variant {
+  int n;        // MMA N (0: no MMA)
+  int ncp;      // scale-factor copies per stage
+};
+
+__global__ void __launch_bounds__(128, 1) rate_kernel(Variant v, unsigned long long* cycles, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t done_bar, stage_bar;
+  __shared__ uint32_t tmem_base_s;
+  for (int i = threadIdx.x; i < kUsed / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0x22222222u, 0x22222222u, 0x38383838u, 0x38383838u);
+  if (threadIdx.x == 0) {
+    mbar_init(&done_bar, 1);
+    mbar_init(&stage_bar, 1);
+    fence_barrier_init();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (threadIdx.x < 32) tmem_alloc(&tmem_base_s, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  if (threadIdx.x == 0) {
+    const uint32_t idesc = idesc_mxf4nvf4(128, v.n > 0 ? v.n : 128);
+    const uint64_t adesc = desc_kmajor_sw128(smem_u32(smem + kOffA));
+    const uint64_t bdesc = desc_kmajor_sw128(smem_u32(smem + kOffB));
+    const uint32_t sfa = tmem + 256, sfb = tmem + 256 + 16;    // columns 256..271 (A), 272..319 (B)
+    const unsigned long long t0 = clock64();
+    for (int s = 0; s < kStages; ++s) {
+      for (int c = 0; c < v.ncp; ++c)
+        tmem_cp_sf_atom(tmem + 256 + 4 * c, desc_sf_atom(smem_u32(smem + kOffSF + 512 * c)));
+      if (v.n > 0) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_mxf4nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, sfa + kk * 4,
+                       sfb + kk * 8, s > 0 || kk > 0);
+      }
+      tc_commit(&stage_bar);       // as the GEMM's per-stage release (nobody waits on it)
+    }
+    tc_commit(&done_bar);
+    const bool ok = wait_parity(&done_bar, 0);
+    const unsigned long long t1 = clock64();
+    if (!ok) atomicExch(err, 1);
+    cycles[blockIdx.x] = t1 - t0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+int main() {
+  int nsm = 0;
+  CK(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, 0));
+  unsigned long long* cyc;
+  int* err;
+  CK(cudaMalloc(&cyc, nsm * sizeof(unsigned long long)));
+  CK(cudaMalloc(&err, sizeof(int)));
+  CK(cudaMemset(err, 0, sizeof(int)));
+  CK(cudaFuncSetAttribute(rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
+  const Variant vs[] = {{128, 0}, {256, 0}, {0, 8}, {128, 8}, {256, 12}, {128, 4}, {256, 8}};
+  const char* names[] = {"mma N=128", "mma N=256", "cp x8", "cp x8 + mma N=128", "cp x12 + mma N=256",
+                         "cp x4 + mma N=128", "cp x8 + mma N=256"};
+  unsigned long long h[1024];
+  if (nsm > 1024) return 1;
+  for (int i = 0; i < 7; ++i) {
+    rate_kernel<<<nsm, 128, kSmem>>>(vs[i], cyc, err);   // warm-up
+    CK(cudaGetLastError());
+    rate_kernel<<<nsm, 128, kSmem>>>(vs[i], cyc, err);
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(h, cyc, nsm * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+    double mean = 0;
+    for (int b = 0; b < nsm; ++b) mean += (double)h[b];
+    mean /= nsm;
+    const double per = mean / kStages;
+    const double flop = vs[i].n > 0 ? 2.0 * 128 * vs[i].n * 256 : 0;
+    printf("%-22s %8.1f cycles per K=256 stage  %8.0f FLOP/cycle/SM  (%.2f PFLOP/s at 148 SMs x 2.032 GHz)\n",
+           names[i], per, flop / per, flop / per * 148 * 2.032e9 / 1e15);
+  }
+  int e;
+  CK(cudaMemcpy(&e, err, sizeof(int), cudaMemcpyDeviceToHost));
+  printf("err=%d\n", e);
+  return e != 0;
+}

@@ -2,9 +2,9 @@
 
     python nvfp4_expert_ffn_gemv_b300/microbench/run.py [name ...]
 
-Names: sync_burst_reduce, handoff, burst_issue (default: all).  Each prints
-its measurements; profiles/sync_handoff_burst_microbench.txt summarises one
-run.  Binaries go to _build/microbench/.
+Names: sync_burst_reduce, handoff, burst_issue, reduce_patterns, tma_stream, mma_rate
+(default: all).  Each prints its measurements; the summaries under profiles/
+quote them.  Binaries go to _build/microbench/.
 """
 import os
 import subprocess
@@ -12,7 +12,7 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 OUT = os.path.join(os.path.dirname(os.path.dirname(HERE)), "_build", "microbench")
-NAMES = ("sync_burst_reduce", "handoff", "burst_issue")
+NAMES = ("sync_burst_reduce", "handoff", "burst_issue", "reduce_patterns", "tma_stream", "mma_rate")
 
 
 def main(names):
