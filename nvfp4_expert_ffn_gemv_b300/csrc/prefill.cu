@@ -68,7 +68,8 @@ constexpr uint32_t kTmemCols = 512;
 // (SFA) and one of weight-side scales (SFB), 16 columns per stage each (a
 // k-step of 64 values of K takes 4 columns of scales per operand).
 constexpr int kSfaCol0 = 2 * kBN;
-constexpr int kSfbCol0 = kSfaCol0 + 128;
+constexpr int kSfaCols = 128;
+constexpr int kSfbCol0 = kSfaCol0 + kSfaCols;
 constexpr int kSfColsPerStage = 16;
 
 // shared-memory plan of the GEMM kernel (offsets from a 1024-aligned base)
@@ -88,7 +89,7 @@ struct Plan {
   static constexpr int offSFB = offSFA + NST * kSF;
   static constexpr int offEpi = offSFB + NST * kSF;
   static_assert(kSfbCol0 + NST * kSfColsPerStage <= (int)kTmemCols, "scale-factor columns exceed TMEM");
-  static_assert(NST * kSfColsPerStage <= kSfbCol0 - kSfaCol0, "SFA ring overlaps SFB");
+  static_assert(NST * kSfColsPerStage <= kSfaCols, "SFA ring overlaps SFB");
 };
 constexpr int kSmemGateUp = Plan<kStagesGateUp>::offEpi + 1024;               // + alignment slack
 constexpr int kSmemDown = Plan<kStagesDown>::offEpi + kEpiBytes + 1024;
@@ -334,6 +335,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int U = (tab.ppos[na] / kBM) * ntiles;
 
 
+
   auto bounded_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (abort_flag) return false;
     if (wait_parity(bar, parity)) return true;
@@ -408,7 +410,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* stage_rows = smem + P::offEpi + (warp - 2) * 32 * kEpiStride;
     int i = 0;
     // Every epilogue warp runs the same units and never leaves the loop early
-    // (a failed wait only skips the work), so all of them always arrive.
+    // (a failed wait only skips the work), so all of them always arrive.  A
+    // warp frees the accumulator as soon as its columns are in registers, so
+    // the next tile's MMAs overlap this tile's arithmetic and stores.
+    auto release = [&](bool ok, int buf) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(&dempty_bar[buf]);
+    };
     for (int u = blockIdx.x; u < U; u += gridDim.x, ++i) {
       const UnitInfo ui = decode_unit(tab, u, ntiles, na);
       const int buf = i & 1;
@@ -429,6 +438,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) { gv[j] = 0u; uv[j] = 0u; }
         }
+        release(ok, buf);
         float hv[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -443,7 +453,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           *reinterpret_cast<uint16_t*>(g.hq_sf + sf_atom_offset(p, ui.ntile * 4, g.f / 64) + 2 * hsel) =
               static_cast<uint16_t>(s0 | (s1 << 8));
         }
-      } else if (ok) {
+      } else {
         // weighted scatter-combine: w * ts_down * D is added into the token's
         // row of the fp32 accumulator (vector reductions in L2; the order in
         // which a token's top_k + shared contributions arrive is not fixed).
@@ -454,18 +464,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const bool acc = g.yacc != nullptr;
         const int row_out = !real ? 0 : acc ? __ldg(g.r.pos_tok + pos) : pos;
         const float wtd = (real && acc) ? __ldg(g.r.pos_w + pos) * ts[2] : ts[2];
-        const unsigned real_mask = __ballot_sync(0xffffffffu, real);
+        const unsigned real_mask = ok ? __ballot_sync(0xffffffffu, real) : 0u;
         float* base = (acc ? g.yacc : g.yexp) + ui.ntile * kBN;
-#pragma unroll 1
-        for (int c0 = hsel * 64; c0 < hsel * 64 + 64; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(taddr + c0, v);
+        uint32_t v[2][32];
+        if (ok) {
+          tmem_ld32(taddr + hsel * 64, v[0]);
+          tmem_ld32(taddr + hsel * 64 + 32, v[1]);
+        }
+        release(ok, buf);
+#pragma unroll
+        for (int h = 0; h < 2 && ok; ++h) {
+          const int c0 = hsel * 64 + h * 32;
           __syncwarp();                         // the previous chunk's rows have been read
 #pragma unroll
           for (int j = 0; j < 32; j += 4)
             *reinterpret_cast<float4*>(stage_rows + lane * kEpiStride + j * 4) =
-                make_float4(__uint_as_float(v[j]) * wtd, __uint_as_float(v[j + 1]) * wtd,
-                            __uint_as_float(v[j + 2]) * wtd, __uint_as_float(v[j + 3]) * wtd);
+                make_float4(__uint_as_float(v[h][j]) * wtd, __uint_as_float(v[h][j + 1]) * wtd,
+                            __uint_as_float(v[h][j + 2]) * wtd, __uint_as_float(v[h][j + 3]) * wtd);
           __syncwarp();
           // 8 lanes per row: each instruction covers 4 rows x 128 contiguous bytes
 #pragma unroll
@@ -484,9 +499,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && ok) mbar_arrive(&dempty_bar[buf]);
     }
   }
 
