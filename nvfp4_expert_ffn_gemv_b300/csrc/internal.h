@@ -119,6 +119,9 @@ cudaError_t prepare_decode_kernels(const moe_ctx* c);
 bool mma_decode_supported(const moe_config& c);
 cudaError_t prepare_mma_decode(const moe_ctx* c);
 cudaError_t launch_mma_decode(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s);
+// 2-D byte tensor map [rows][row_bytes] with boxes of box_bytes x box_rows (prefill.cu)
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_bytes,
+                  uint32_t box_rows, bool swizzle128);
 bool prefill_supported(const moe_config& c);
 bool prefill_accumulates(const moe_config& c, int T);
 size_t prefill_max_rows(const moe_config& c);
