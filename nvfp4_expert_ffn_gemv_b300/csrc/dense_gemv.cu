@@ -57,6 +57,7 @@ struct GemvArgs {
   int T;                   // tokens of this pass (<= kTokPass)
   float ts0, ts1;          // tensor scales (head: ts0; gate/up: ts0 gate, ts1 up; down: ts0)
   float* out;              // head [T][out_ld] logits; gate/up [T][out_ld] h; down [S][T][out_ld] partials
+  uint32_t* hmax;          // gate/up: max |h| of each token (fp32 bits), folded in with atomicMax
   int out_ld;
   int nstages;             // stages = consumer warps
   int* status;
@@ -204,6 +205,26 @@ __device__ __forceinline__ void consume_unit(const GemvArgs& g, const uint8_t* s
       }
     }
   }
+  if (MODE == kModeGateUp) {
+    // max |h| per token over this unit's 8 hidden units (the 8 lanes gq of each
+    // c hold them), folded into the token's word; NaN is left out, as fmaxf does
+#pragma unroll
+    for (int q = 0; q < NG; ++q)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int t = 8 * q + 2 * c + j;
+        float a = 0.f;
+        if (t < g.T) {
+          const float hv = silu_f(acc[0][q][j] * g.ts0 * g.unshift[t]) * (acc[0][q][2 + j] * g.ts1 * g.unshift[t]);
+          a = fabsf(hv) == fabsf(hv) ? fabsf(hv) : 0.f;
+        }
+        uint32_t m = __float_as_uint(a);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        if (gq == 0 && t < g.T && m != 0u) atomicMax(g.hmax + t, m);
+      }
+  }
 }
 
 template <int MODE>
@@ -285,9 +306,11 @@ __device__ __forceinline__ float block_max256(float m, uint32_t* red) {
 // bf16 x [T][K] -> prescaled f16 in the permuted chunk order, one CTA per row
 // of the B operand (rows T .. rows_read(T) - 1 zero); unshift[t] = 2^-shift.
 __global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int K,
-                                                     uint8_t* __restrict__ out, float* __restrict__ unshift) {
+                                                     uint8_t* __restrict__ out, float* __restrict__ unshift,
+                                                     uint32_t* __restrict__ hmax) {
   __shared__ uint32_t red[8];
   const int t = blockIdx.x;
+  if (hmax && threadIdx.x == 0) hmax[t] = 0u;   // the dense FFN's gate/up pass folds max |h| in here
   uint8_t* dst = out + (size_t)t * K * 2;
   if (t >= T) {
     for (int i = threadIdx.x; i < K / 8; i += 256) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -322,30 +345,32 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* __rest
   if (threadIdx.x == 0) unshift[t] = pow2i(-shift);
 }
 
-// fp32 h [T][K] -> prescaled f16 hi + lo in the permuted chunk order, one CTA per row (rows T.. zero).
-__global__ void __launch_bounds__(256) prep_h_kernel(const float* __restrict__ h, int T, int K, uint8_t* __restrict__ hi,
+// fp32 h [T][K] -> prescaled f16 hi + lo in the permuted chunk order.  The
+// prescale comes from the token's max |h|, which the gate/up pass folded into
+// hmax[t], so a row is split over K / 2048 CTAs (blockIdx.x = chunk,
+// blockIdx.y = row; rows T.. are zero).
+constexpr int kPrepHChunk = 2048;
+__global__ void __launch_bounds__(256) prep_h_kernel(const float* __restrict__ h, int T, int K,
+                                                     const uint32_t* __restrict__ hmax, uint8_t* __restrict__ hi,
                                                      uint8_t* __restrict__ lo, float* __restrict__ unshift) {
-  __shared__ uint32_t red[8];
-  const int t = blockIdx.x;
+  const int t = blockIdx.y;
+  const int i0 = blockIdx.x * (kPrepHChunk / 4), i1 = min(K / 4, i0 + kPrepHChunk / 4);
   uint8_t* dh = hi + (size_t)t * K * 2;
   uint8_t* dl = lo + (size_t)t * K * 2;
   if (t >= T) {
-    for (int i = threadIdx.x; i < K / 8; i += 256) {
-      reinterpret_cast<uint4*>(dh)[i] = make_uint4(0u, 0u, 0u, 0u);
-      reinterpret_cast<uint4*>(dl)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = i0 + (int)threadIdx.x; i < i1; i += 256) {
+      const int k0 = 4 * i, kp = k0 % 128;
+      const size_t off = (size_t)(k0 / 128) * 256 + perm_off(kp / 32, (kp % 32) / 4);
+      *reinterpret_cast<uint2*>(dh + off) = make_uint2(0u, 0u);
+      *reinterpret_cast<uint2*>(dl + off) = make_uint2(0u, 0u);
     }
-    if (threadIdx.x == 0) unshift[t] = 0.f;
+    if (blockIdx.x == 0 && threadIdx.x == 0) unshift[t] = 0.f;
     return;
   }
-  const float4* src = reinterpret_cast<const float4*>(h + (size_t)t * K);
-  float m = 0.f;
-  for (int i = threadIdx.x; i < K / 4; i += 256) {
-    const float4 v = src[i];
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-  }
-  const int shift = prescale_shift(__float_as_uint(block_max256(m, red)));
+  const int shift = prescale_shift(hmax[t]);
   const float sc = pow2i(shift);
-  for (int i = threadIdx.x; i < K / 4; i += 256) {
+  const float4* src = reinterpret_cast<const float4*>(h + (size_t)t * K);
+  for (int i = i0 + (int)threadIdx.x; i < i1; i += 256) {
     const float4 v = src[i];
     uint2 vh, vl;
     split_hi_lo(v.x * sc, v.y * sc, v.z * sc, v.w * sc, vh, vl);
@@ -354,7 +379,7 @@ __global__ void __launch_bounds__(256) prep_h_kernel(const float* __restrict__ h
     *reinterpret_cast<uint2*>(dh + off) = vh;
     *reinterpret_cast<uint2*>(dl + off) = vl;
   }
-  if (threadIdx.x == 0) unshift[t] = pow2i(-shift);
+  if (blockIdx.x == 0 && threadIdx.x == 0) unshift[t] = pow2i(-shift);
 }
 
 // y[t][r] = bf16(sum over the S K slices, in order, of partial[s][t][r] (+ x[t][r]))
@@ -447,6 +472,7 @@ struct moe_dense {
   uint8_t* h_hi = nullptr;   // FFN: [kTokPass][f] f16
   uint8_t* h_lo = nullptr;
   float* hun = nullptr;      // FFN: [kTokPass]
+  uint32_t* hmax = nullptr;  // FFN: [kTokPass] max |h| of each token (fp32 bits)
   float* part = nullptr;     // FFN: [S][kTokPass][d]
   int* status = nullptr;
 };
@@ -478,6 +504,7 @@ size_t carve_dense(moe_dense* x, uint8_t* base) {
     x->h_hi = take((size_t)kTokPass * f * 2);
     x->h_lo = take((size_t)kTokPass * f * 2);
     x->hun = reinterpret_cast<float*>(take(kTokPass * sizeof(float)));
+    x->hmax = reinterpret_cast<uint32_t*>(take(kTokPass * sizeof(uint32_t)));
     x->part = reinterpret_cast<float*>(take((size_t)x->S * kTokPass * d * sizeof(float)));
   }
   return off;
@@ -486,9 +513,10 @@ size_t carve_dense(moe_dense* x, uint8_t* base) {
 bool matrix_ok(const moe_matrix* m) { return m && m->codes && m->scales && m->tensor_scale; }
 
 // K slices of the dense down projection: the largest K slice <= 2304 that is a
-// multiple of 128 and divides f (so a stage of 16 rows x K slice stays ~20 KB)
+// multiple of 256 (a code row of the slice is whole 128-byte swizzle segments)
+// and divides f (so a stage of 16 rows x K slice stays ~20 KB).
 int down_slices(int f) {
-  for (int ks = 2304; ks >= 128; ks -= 128)
+  for (int ks = 2304; ks >= 256; ks -= 256)
     if (f % ks == 0) return f / ks;
   return -1;
 }
@@ -591,7 +619,7 @@ moe_status moe_head_forward(moe_dense* x, const void* x_bf16, int T, float* logi
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x_bf16);
   for (int t0 = 0; t0 < T; t0 += kTokPass) {
     const int n = T - t0 < kTokPass ? T - t0 : kTokPass;
-    prep_x_kernel<<<rows_read(n), 256, 0, s>>>(xb + (size_t)t0 * x->d, n, x->d, x->x16, x->xun);
+    prep_x_kernel<<<rows_read(n), 256, 0, s>>>(xb + (size_t)t0 * x->d, n, x->d, x->x16, x->xun, nullptr);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     GemvArgs g = base_args(x, n);
     g.codes = x->codes;
@@ -697,7 +725,7 @@ moe_status moe_ffn_forward(moe_dense* x, const void* x_bf16, int T, void* y_bf16
   const int d = x->d, f = x->f;
   for (int t0 = 0; t0 < T; t0 += kTokPass) {
     const int n = T - t0 < kTokPass ? T - t0 : kTokPass;
-    prep_x_kernel<<<rows_read(n), 256, 0, s>>>(xb + (size_t)t0 * d, n, d, x->x16, x->xun);
+    prep_x_kernel<<<rows_read(n), 256, 0, s>>>(xb + (size_t)t0 * d, n, d, x->x16, x->xun, x->hmax);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     GemvArgs g = base_args(x, n);
     g.codes = x->codes;
@@ -711,8 +739,10 @@ moe_status moe_ffn_forward(moe_dense* x, const void* x_bf16, int T, void* y_bf16
     g.ts1 = x->ts[1];
     g.out = x->h;
     g.out_ld = f;
+    g.hmax = x->hmax;
     if (launch_gemv<kModeGateUp>(g, x->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
-    prep_h_kernel<<<rows_read(n), 256, 0, s>>>(x->h, n, f, x->h_hi, x->h_lo, x->hun);
+    prep_h_kernel<<<dim3((unsigned)((f + kPrepHChunk - 1) / kPrepHChunk), (unsigned)rows_read(n)), 256, 0, s>>>(
+        x->h, n, f, x->hmax, x->h_hi, x->h_lo, x->hun);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     GemvArgs dn = base_args(x, n);
     dn.codes = x->dn_codes;
