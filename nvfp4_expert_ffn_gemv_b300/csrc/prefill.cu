@@ -14,12 +14,13 @@
 //   2. x -> NVFP4 (16-element E4M3 block scales, tensor scale 1) gathered into
 //              the padded blocks, scales written straight into the
 //              scale-factor atoms the MMA reads;
-//   3. GEMM gate/up: D[128 tokens, 128 weight rows] per (token block, 128-row
-//              tile of the gate/up layout).  Such a tile holds 64 gate rows
-//              and the matching 64 up rows, so each epilogue thread (one
-//              token, one TMEM lane) forms h = silu(g) * u for 64 hidden units
-//              in registers and quantises it to NVFP4 (block 16, scale 1):
-//              32 contiguous code bytes and 4 adjacent scale bytes per token;
+//   3. GEMM gate/up: D[128 tokens, 256 weight rows] per (token block, 256-row
+//              tile of the gate/up layout).  Such a tile holds two groups of
+//              64 gate rows and the matching 64 up rows, so each epilogue
+//              thread (one token, one TMEM lane) forms h = silu(g) * u for its
+//              32 hidden units in registers and quantises it to NVFP4 (block
+//              16, scale 1): 16 contiguous code bytes and 2 adjacent scale
+//              bytes per token;
 //   4. GEMM down: D[128 tokens, 128 output dims] * ts_down * w is added with
 //              vector reductions into the token's row of an fp32 accumulator
 //              that stays in L2 (the weighted scatter-combine; the order of a
@@ -28,20 +29,25 @@
 //              fit well inside L2 store per-position outputs instead and add
 //              them in a fixed order afterwards.
 //
-// GEMM kernel: persistent, one CTA (320 threads) per SM, 512 TMEM columns
-// (two 128-column accumulators, so the epilogue of one tile overlaps the MMAs
-// of the next, plus 32 scale-factor columns per stage).
-//   warp 0  TMA producer: ring of {A 128x256 fp4 tokens (SW128),
-//           B 128x256 fp4 weights (SW128), SFA 4 atoms, SFB 4 atoms}, 6 stages
-//           in the gate/up GEMM, 4 in the down GEMM (whose epilogue needs
-//           shared memory too)
+// GEMM kernel: persistent, one CTA per SM, 512 TMEM columns.
+//   gate/up: 128 x 256 tiles (an N = 256 MMA costs 40% more than an N = 128
+//            one for twice the work, and its 12 scale copies per stage are 6
+//            per 128 columns instead of 8), one 256-column accumulator, 576
+//            threads; the epilogue warps free it as soon as their columns are
+//            in registers, so the next tile's MMAs wait only for those loads;
+//   down:    128 x 128 tiles, two 128-column accumulators (the epilogue of one
+//            tile overlaps the MMAs of the next), 320 threads.
+//   warp 0  TMA producer: 4-stage ring of {A 128x256 fp4 tokens (SW128),
+//           B 128 or 256 x 256 fp4 weights (SW128), SFA 4 atoms, SFB 4 atoms
+//           per 128 rows}
 //   warp 1  TMEM owner + single-thread MMA issuer: per stage, scale atoms ->
 //           TMEM (tcgen05.cp 32x128b.warpx4), 4 MMAs of K = 64
-//   warps 2-9 epilogue: two warps per TMEM lane quarter (lanes 32*(warp%4) ..),
-//           each taking half of the tile's columns (tcgen05.ld 32 at a time).
-//           The down GEMM's rows go through a per-warp shared-memory tile so
-//           that each vector reduction covers 4 rows x 128 contiguous bytes
-//           instead of 32 scattered rows (2x the reduction rate into L2).
+//   warps 2.. epilogue: BN / 64 warps per TMEM lane quarter (lanes
+//           32*(warp%4) ..), 32 columns of each 64-column half each
+//           (tcgen05.ld 32 at a time).  The down GEMM's rows go through a
+//           per-warp shared-memory tile so that each vector reduction covers
+//           4 rows x 128 contiguous bytes instead of 32 scattered rows (2x the
+//           reduction rate into L2).
 // All waits are bounded; the first one that gives up latches MOE_ERR_TIMEOUT
 // and sets a CTA-wide abort flag so that no other role waits afterwards.
 #include <cuda.h>
@@ -57,42 +63,49 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128;        // tokens per tile (MMA M, TMEM lanes)
-constexpr int kBN = 128;        // weight rows per tile (MMA N)
 constexpr int kStageK = 256;    // fp4 elements of K per stage (128 bytes per row)
-constexpr int kStagesGateUp = 6;   // gate/up: 6 x 36 KB in flight (no epilogue staging)
+constexpr int kBNGateUp = 256;  // gate/up: 128 tokens x 256 weight rows per tile
+constexpr int kBNDown = 128;    // down: 128 tokens x 128 output dims per tile
+constexpr int kStagesGateUp = 4;   // gate/up: 4 x 54 KB in flight
 constexpr int kStagesDown = 4;     // down: 4 x 36 KB + the epilogue's row staging
-constexpr int kEpiWarps = 8;
-constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: two 128-column accumulators, then a ring of token-side scales
-// (SFA) and one of weight-side scales (SFB), 16 columns per stage each (a
-// k-step of 64 values of K takes 4 columns of scales per operand).
-constexpr int kSfaCol0 = 2 * kBN;
-constexpr int kSfaCols = 128;
-constexpr int kSfbCol0 = kSfaCol0 + kSfaCols;
-constexpr int kSfColsPerStage = 16;
+constexpr int kSfColsPerStage = 16;           // 4 k-steps x 4 columns of scales per 128 rows
 
 // shared-memory plan of the GEMM kernel (offsets from a 1024-aligned base)
 constexpr int kA = kBM * 128;                 // 16 KB per stage
-constexpr int kB = kBN * 128;                 // 16 KB per stage
-constexpr int kSF = 4 * 512;                  // 2 KB per operand per stage
-constexpr int kStageBytes = kA + kB + 2 * kSF;
+constexpr int kSF = 4 * 512;                  // 2 KB of scales per 128 rows per stage
 constexpr int kEpiStride = 144;             // staged row: 32 fp32 + 16 bytes of padding (no bank conflicts)
-constexpr int kEpiBytes = kEpiWarps * 32 * kEpiStride;
-// ring of NST stages {A, B, SFA, SFB} from a 1024-aligned base, then (down
-// GEMM only) the epilogue's staging rows
-template <int NST>
+// Tile of BN weight rows: epilogue warps (two per 64 columns, 32 columns
+// each: BN / 16 warps), threads, the ring of NST stages {A, B, SFA, SFB}
+// from a 1024-aligned base and (down GEMM only) the epilogue's staging rows.
+// TMEM: the accumulator(s) (two of 128 columns for BN = 128 so that a tile's
+// epilogue overlaps the next tile's MMAs; one of 256 for BN = 256), then a
+// ring of token-side scales (16 columns per stage) and one of weight-side
+// scales (16 columns per 128 rows per stage: a k-step takes 4 columns per
+// 128 rows, rows 128..255 of a 256-row tile in the 4 columns after rows
+// 0..127).
+template <int NST, int BN>
 struct Plan {
+  static constexpr int epi_warps = BN / 16;
+  static constexpr int threads = 64 + 32 * epi_warps;
+  static constexpr int kB = BN * 128;
+  static constexpr int kSFB = (BN / 128) * kSF;
+  static constexpr int stage_bytes = kA + kB + kSF + kSFB;
   static constexpr int offA = 0;
   static constexpr int offB = offA + NST * kA;
   static constexpr int offSFA = offB + NST * kB;
   static constexpr int offSFB = offSFA + NST * kSF;
-  static constexpr int offEpi = offSFB + NST * kSF;
-  static_assert(kSfbCol0 + NST * kSfColsPerStage <= (int)kTmemCols, "scale-factor columns exceed TMEM");
-  static_assert(NST * kSfColsPerStage <= kSfaCols, "SFA ring overlaps SFB");
+  static constexpr int offEpi = offSFB + NST * kSFB;
+  static constexpr int nacc = BN == 256 ? 1 : 2;
+  static constexpr int sfaCol0 = nacc * BN;
+  static constexpr int sfbCol0 = sfaCol0 + NST * kSfColsPerStage;
+  static constexpr int sfbColsPerStage = (BN / 128) * kSfColsPerStage;
+  static_assert(sfbCol0 + NST * sfbColsPerStage <= (int)kTmemCols, "scale-factor columns exceed TMEM");
 };
-constexpr int kSmemGateUp = Plan<kStagesGateUp>::offEpi + 1024;               // + alignment slack
-constexpr int kSmemDown = Plan<kStagesDown>::offEpi + kEpiBytes + 1024;
+using PlanGateUp = Plan<kStagesGateUp, kBNGateUp>;
+using PlanDown = Plan<kStagesDown, kBNDown>;
+constexpr int kSmemGateUp = PlanGateUp::offEpi + 1024;               // + alignment slack
+constexpr int kSmemDown = PlanDown::offEpi + PlanDown::epi_warps * 32 * kEpiStride + 1024;
 
 // largest a < na with tab[a] <= v (tab non-decreasing, tab[0] = 0)
 __device__ __forceinline__ int find_seg(const int32_t* tab, int na, int v) {
@@ -289,11 +302,12 @@ __device__ __forceinline__ uint32_t quant16(const float* v, uint2& codes) {
   return s;
 }
 
-template <int NST, int MODE>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int NST, int MODE, int BN>
+__global__ void __launch_bounds__(Plan<NST, BN>::threads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
-  using P = Plan<NST>;
+  using P = Plan<NST, BN>;
+  constexpr int kEpi = P::epi_warps;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full_bar[NST], empty_bar[NST], dfull_bar[2], dempty_bar[2];
   __shared__ uint32_t tmem_base_s;
@@ -309,7 +323,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tab.pos[i] = g.r.act_pos[i];
     }
   }
-  const int ntiles = g.M / kBN, ksteps = g.K / 64, kstages = g.K / kStageK;
+  const int ntiles = g.M / BN, ksteps = g.K / 64, kstages = g.K / kStageK;
+  const int mtiles = g.M / 128;   // 128-row tiles of scale atoms per expert
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -318,7 +333,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&dfull_bar[b], 1);
-      mbar_init(&dempty_bar[b], kEpiWarps);
+      mbar_init(&dempty_bar[b], kEpi);
     }
     abort_flag = 0;
     fence_barrier_init();
@@ -351,16 +366,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
         const UnitInfo ui = decode_unit(tab, u, ntiles, na);
-        const int brow = ui.e * g.M + ui.ntile * kBN;
+        const int brow = ui.e * g.M + ui.ntile * BN;
         const uint8_t* sfa = g.sfa + (size_t)(ui.p0 / kBM) * ksteps * 512;
-        const uint8_t* sfb = g.sfb + ((size_t)ui.e * ntiles + ui.ntile) * ksteps * 512;
+        const uint8_t* sfb = g.sfb + ((size_t)ui.e * mtiles + ui.ntile * (BN / 128)) * ksteps * 512;
         for (int ks = 0; ks < kstages; ++ks) {
           if (!bounded_wait(&empty_bar[stage], phase ^ 1)) break;
-          mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+          mbar_arrive_expect_tx(&full_bar[stage], P::stage_bytes);
           tma_load_2d(smem + P::offA + stage * kA, &tmA, ks * 128, ui.p0, &full_bar[stage]);
-          tma_load_2d(smem + P::offB + stage * kB, &tmB, ks * 128, brow, &full_bar[stage]);
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            tma_load_2d(smem + P::offB + stage * P::kB + h * 128 * 128, &tmB, ks * 128, brow + h * 128,
+                        &full_bar[stage]);
           bulk_load(smem + P::offSFA + stage * kSF, sfa + (size_t)ks * 4 * 512, kSF, &full_bar[stage]);
-          bulk_load(smem + P::offSFB + stage * kSF, sfb + (size_t)ks * 4 * 512, kSF, &full_bar[stage]);
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            bulk_load(smem + P::offSFB + stage * P::kSFB + h * kSF, sfb + ((size_t)h * ksteps + ks * 4) * 512, kSF,
+                      &full_bar[stage]);
           if (++stage == NST) { stage = 0; phase ^= 1; }
         }
       }
@@ -370,31 +391,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      const uint32_t idesc = idesc_mxf4nvf4(kBM, kBN);
+      const uint32_t idesc = idesc_mxf4nvf4(kBM, BN);
       int i = 0;
       for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x, ++i) {
-        const int buf = i & 1;
-        if (!bounded_wait(&dempty_bar[buf], ((i >> 1) & 1) ^ 1)) break;
+        const int buf = i % P::nacc, use = i / P::nacc;
+        if (!bounded_wait(&dempty_bar[buf], (use & 1) ^ 1)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * kBN;
+        const uint32_t d_tmem = tmem + buf * BN;
         for (int ks = 0; ks < kstages; ++ks) {
           if (!bounded_wait(&full_bar[stage], phase)) break;
           tc_fence_after();
-          const uint32_t sfa_t = tmem + kSfaCol0 + stage * kSfColsPerStage;
-          const uint32_t sfb_t = tmem + kSfbCol0 + stage * kSfColsPerStage;
+          const uint32_t sfa_t = tmem + P::sfaCol0 + stage * kSfColsPerStage;
+          const uint32_t sfb_t = tmem + P::sfbCol0 + stage * P::sfbColsPerStage;
           const uint32_t sa = smem_u32(smem + P::offSFA + stage * kSF);
-          const uint32_t sb = smem_u32(smem + P::offSFB + stage * kSF);
+          const uint32_t sb = smem_u32(smem + P::offSFB + stage * P::kSFB);
+          // k-step kk: SFA in 4 columns; SFB of rows 128h .. 128h+127 in the
+          // 4 columns at kk * 4 * (BN / 128) + 4h
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             tmem_cp_sf_atom(sfa_t + kk * 4, desc_sf_atom(sa + kk * 512));
-            tmem_cp_sf_atom(sfb_t + kk * 4, desc_sf_atom(sb + kk * 512));
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tmem_cp_sf_atom(sfb_t + kk * 4 * (BN / 128) + h * 4, desc_sf_atom(sb + h * kSF + kk * 512));
           }
           const uint64_t adesc = desc_kmajor_sw128(smem_u32(smem + P::offA + stage * kA));
-          const uint64_t bdesc = desc_kmajor_sw128(smem_u32(smem + P::offB + stage * kB));
+          const uint64_t bdesc = desc_kmajor_sw128(smem_u32(smem + P::offB + stage * P::kB));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_mxf4nvf4(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, sfa_t + kk * 4,
-                         sfb_t + kk * 4, ks > 0 || kk > 0);
+                         sfb_t + kk * 4 * (BN / 128), ks > 0 || kk > 0);
           tc_commit(&empty_bar[stage]);
           if (++stage == NST) { stage = 0; phase ^= 1; }
         }
@@ -404,8 +429,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------ epilogue ------------------------------
     // TMEM lane = token row of the block; this thread owns token row m and
-    // column half hsel of the tile.
-    const int q = warp & 3, hsel = (warp - 2) >> 2;
+    // the 32-column slice `sub` of each 64-column half of a 128-column group.
+    const int q = warp & 3, sub = (warp - 2) >> 2;
     const int m = q * 32 + lane;
     uint8_t* stage_rows = smem + P::offEpi + (warp - 2) * 32 * kEpiStride;
     int i = 0;
@@ -420,20 +445,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     };
     for (int u = blockIdx.x; u < U; u += gridDim.x, ++i) {
       const UnitInfo ui = decode_unit(tab, u, ntiles, na);
-      const int buf = i & 1;
-      const bool ok = __all_sync(0xffffffffu, bounded_wait(&dfull_bar[buf], (i >> 1) & 1));   // warp-uniform
+      const int buf = i % P::nacc, use = i / P::nacc;
+      const bool ok = __all_sync(0xffffffffu, bounded_wait(&dfull_bar[buf], use & 1));   // warp-uniform
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * kBN;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * BN;
       const float* ts = g.tsc + ui.e * 3;
       const int p = ui.p0 + m;                    // padded row of this token
       if constexpr (MODE == 0) {
-        // columns 0..63 gate rows, 64..127 up rows of hidden units 64*ntile + 0..63;
-        // this warp forms hidden units 32*hsel .. 32*hsel+31
+        // 128-column group grp holds 64 gate rows then the matching 64 up rows
+        // of hidden units (BN / 2) * ntile + 64 * grp + 0..63; this warp forms
+        // the 32 of them at 32 * h32
+        const int grp = sub >> 1, h32 = sub & 1;
+        const int hid0 = 64 * grp + 32 * h32;   // first hidden unit of the warp within the tile
         const float tg = ts[0], tu = ts[1];
         uint32_t gv[32], uv[32];
         if (ok) {
-          tmem_ld32(taddr + hsel * 32, gv);
-          tmem_ld32(taddr + 64 + hsel * 32, uv);
+          tmem_ld32(taddr + 128 * grp + 32 * h32, gv);
+          tmem_ld32(taddr + 128 * grp + 64 + 32 * h32, uv);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) { gv[j] = 0u; uv[j] = 0u; }
@@ -446,11 +474,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint2 c0, c1;
         const uint32_t s0 = quant16(hv, c0), s1 = quant16(hv + 16, c1);
         if (ok) {
-          *reinterpret_cast<uint4*>(g.hq_codes + (size_t)p * (g.f / 2) + ui.ntile * 32 + hsel * 16) =
-              make_uint4(c0.x, c0.y, c1.x, c1.y);
-          // the 4 block scales of these 64 hidden units are one k-step of the
-          // down GEMM (4 adjacent bytes); this warp writes two of them
-          *reinterpret_cast<uint16_t*>(g.hq_sf + sf_atom_offset(p, ui.ntile * 4, g.f / 64) + 2 * hsel) =
+          const int hb = ui.ntile * (BN / 2) + hid0;   // first hidden unit
+          *reinterpret_cast<uint4*>(g.hq_codes + (size_t)p * (g.f / 2) + hb / 2) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+          // its two 16-unit block scales: 2 adjacent bytes of one k-step atom of the down GEMM
+          *reinterpret_cast<uint16_t*>(g.hq_sf + sf_atom_offset(p, hb / 16, g.f / 64)) =
               static_cast<uint16_t>(s0 | (s1 << 8));
         }
       } else {
@@ -465,16 +492,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int row_out = !real ? 0 : acc ? __ldg(g.r.pos_tok + pos) : pos;
         const float wtd = (real && acc) ? __ldg(g.r.pos_w + pos) * ts[2] : ts[2];
         const unsigned real_mask = ok ? __ballot_sync(0xffffffffu, real) : 0u;
-        float* base = (acc ? g.yacc : g.yexp) + ui.ntile * kBN;
+        float* base = (acc ? g.yacc : g.yexp) + ui.ntile * BN;
         uint32_t v[2][32];
         if (ok) {
-          tmem_ld32(taddr + hsel * 64, v[0]);
-          tmem_ld32(taddr + hsel * 64 + 32, v[1]);
+          tmem_ld32(taddr + sub * 64, v[0]);
+          tmem_ld32(taddr + sub * 64 + 32, v[1]);
         }
         release(ok, buf);
 #pragma unroll
         for (int h = 0; h < 2 && ok; ++h) {
-          const int c0 = hsel * 64 + h * 32;
+          const int c0 = sub * 64 + h * 32;
           __syncwarp();                         // the previous chunk's rows have been read
 #pragma unroll
           for (int j = 0; j < 32; j += 4)
@@ -593,10 +620,10 @@ cudaError_t prefill_prepare(moe_ctx* c) {
             make_tmap(&c->pf_tm[2], c->pf_xq, rows, d / 2, kBM) &&
             make_tmap(&c->pf_tm[3], c->pf_hq, rows, f / 2, kBM);
   if (!ok) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(moe_gemm_kernel<kStagesGateUp, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemGateUp);
+  e = cudaFuncSetAttribute(moe_gemm_kernel<kStagesGateUp, 0, kBNGateUp>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGateUp);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(moe_gemm_kernel<kStagesDown, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(moe_gemm_kernel<kStagesDown, 1, kBNDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemDown);
 }
 
@@ -620,7 +647,8 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   g.K = d;
   g.hq_codes = c->pf_hq;
   g.hq_sf = c->pf_hsf;
-  moe_gemm_kernel<kStagesGateUp, 0><<<c->sm_count, kGemmThreads, kSmemGateUp, s>>>(c->pf_tm[2], c->pf_tm[0], g);
+  moe_gemm_kernel<kStagesGateUp, 0, kBNGateUp>
+      <<<c->sm_count, PlanGateUp::threads, kSmemGateUp, s>>>(c->pf_tm[2], c->pf_tm[0], g);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // down projection -> per-slot outputs
   g.sfa = c->pf_hsf;
@@ -629,7 +657,8 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   g.K = f;
   g.yacc = prefill_accumulates(c->cfg, T) ? c->yacc : nullptr;
   g.yexp = c->yexp;
-  moe_gemm_kernel<kStagesDown, 1><<<c->sm_count, kGemmThreads, kSmemDown, s>>>(c->pf_tm[3], c->pf_tm[1], g);
+  moe_gemm_kernel<kStagesDown, 1, kBNDown>
+      <<<c->sm_count, PlanDown::threads, kSmemDown, s>>>(c->pf_tm[3], c->pf_tm[1], g);
   return cudaGetLastError();
 }
 
