@@ -502,7 +502,7 @@ int moe_kernels_per_forward(moe_ctx* x, int T, int prefill) {
   if (!x || T <= 0) return 0;
   if (!prefill && T == 1 && x->b1_enabled) return 3;
   const int nb = bucket_kernel_count(T);
-  if (prefill) return 7 + nb;   // router x2, bucketing, quantise x, gather x, GEMM x2, finish
+  if (prefill) return 6 + nb;   // router x2, bucketing, quantise + scatter x, GEMM x2, finish
   if (x->mma_enabled) return 6 + nb;   // router x2, bucketing, x prescale, gate/up, down, combine
   return 5 + nb;
 }
