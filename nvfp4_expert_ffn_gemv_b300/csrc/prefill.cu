@@ -36,15 +36,15 @@
 //            threads; the epilogue warps free it as soon as their columns are
 //            in registers, so the next tile's MMAs wait only for those loads;
 //   down:    128 x 128 tiles, two 128-column accumulators (the epilogue of one
-//            tile overlaps the MMAs of the next), 320 threads.
+//            tile overlaps the MMAs of the next), 16 epilogue warps of 32
+//            columns each (the vector reductions are its bound), 576 threads.
 //   warp 0  TMA producer: 4-stage ring of {A 128x256 fp4 tokens (SW128),
 //           B 128 or 256 x 256 fp4 weights (SW128), SFA 4 atoms, SFB 4 atoms
 //           per 128 rows}
 //   warp 1  TMEM owner + single-thread MMA issuer: per stage, scale atoms ->
 //           TMEM (tcgen05.cp 32x128b.warpx4), 4 MMAs of K = 64
-//   warps 2.. epilogue: BN / 64 warps per TMEM lane quarter (lanes
-//           32*(warp%4) ..), 32 columns of each 64-column half each
-//           (tcgen05.ld 32 at a time).  The down GEMM's rows go through a
+//   warps 2.. epilogue: 4 warps per TMEM lane quarter (lanes 32*(warp%4) ..),
+//           tcgen05.ld 32 columns at a time.  The down GEMM's rows go through a
 //           per-warp shared-memory tile so that each vector reduction covers
 //           4 rows x 128 contiguous bytes instead of 32 scattered rows (2x the
 //           reduction rate into L2).
@@ -84,9 +84,9 @@ constexpr int kEpiStride = 144;             // staged row: 32 fp32 + 16 bytes of
 // scales (16 columns per 128 rows per stage: a k-step takes 4 columns per
 // 128 rows, rows 128..255 of a 256-row tile in the 4 columns after rows
 // 0..127).
-template <int NST, int BN>
+template <int NST, int BN, int EW>
 struct Plan {
-  static constexpr int epi_warps = BN / 16;
+  static constexpr int epi_warps = EW;
   static constexpr int threads = 64 + 32 * epi_warps;
   static constexpr int kB = BN * 128;
   static constexpr int kSFB = (BN / 128) * kSF;
@@ -102,8 +102,10 @@ struct Plan {
   static constexpr int sfbColsPerStage = (BN / 128) * kSfColsPerStage;
   static_assert(sfbCol0 + NST * sfbColsPerStage <= (int)kTmemCols, "scale-factor columns exceed TMEM");
 };
-using PlanGateUp = Plan<kStagesGateUp, kBNGateUp>;
-using PlanDown = Plan<kStagesDown, kBNDown>;
+constexpr int kEpiGateUp = kBNGateUp / 16;   // 32 hidden units (64 columns) per warp
+constexpr int kEpiDown = 16;                  // 32 output columns per warp
+using PlanGateUp = Plan<kStagesGateUp, kBNGateUp, kEpiGateUp>;
+using PlanDown = Plan<kStagesDown, kBNDown, kEpiDown>;
 constexpr int kSmemGateUp = PlanGateUp::offEpi + 1024;               // + alignment slack
 constexpr int kSmemDown = PlanDown::offEpi + PlanDown::epi_warps * 32 * kEpiStride + 1024;
 
@@ -302,12 +304,15 @@ __device__ __forceinline__ uint32_t quant16(const float* v, uint2& codes) {
   return s;
 }
 
-template <int NST, int MODE, int BN>
-__global__ void __launch_bounds__(Plan<NST, BN>::threads, 1)
+template <int NST, int MODE, int BN, int EW>
+__global__ void __launch_bounds__(Plan<NST, BN, EW>::threads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
-  using P = Plan<NST, BN>;
+  using P = Plan<NST, BN, EW>;
   constexpr int kEpi = P::epi_warps;
+  static_assert(MODE == 1 || EW == BN / 16, "gate/up: one warp per 32 hidden units of a lane quarter");
+  constexpr int kColsPerWarp = BN * 4 / EW;   // down: output columns of one epilogue warp
+  static_assert(MODE == 0 || kColsPerWarp % 32 == 0, "down: whole 32-column chunks per warp");
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full_bar[NST], empty_bar[NST], dfull_bar[2], dempty_bar[2];
   __shared__ uint32_t tmem_base_s;
@@ -429,7 +434,8 @@ __global__ void __launch_bounds__(Plan<NST, BN>::threads, 1)
   } else {
     // ------------------------------ epilogue ------------------------------
     // TMEM lane = token row of the block; this thread owns token row m and
-    // the 32-column slice `sub` of each 64-column half of a 128-column group.
+    // slice `sub` of the tile (gate/up: 32 hidden units, i.e. 32 gate and 32
+    // up columns; down: kColsPerWarp output columns).
     const int q = warp & 3, sub = (warp - 2) >> 2;
     const int m = q * 32 + lane;
     uint8_t* stage_rows = smem + P::offEpi + (warp - 2) * 32 * kEpiStride;
@@ -493,15 +499,16 @@ __global__ void __launch_bounds__(Plan<NST, BN>::threads, 1)
         const float wtd = (real && acc) ? __ldg(g.r.pos_w + pos) * ts[2] : ts[2];
         const unsigned real_mask = ok ? __ballot_sync(0xffffffffu, real) : 0u;
         float* base = (acc ? g.yacc : g.yexp) + ui.ntile * BN;
-        uint32_t v[2][32];
+        constexpr int kChunks = kColsPerWarp / 32;
+        uint32_t v[kChunks][32];
         if (ok) {
-          tmem_ld32(taddr + sub * 64, v[0]);
-          tmem_ld32(taddr + sub * 64 + 32, v[1]);
+#pragma unroll
+          for (int h = 0; h < kChunks; ++h) tmem_ld32(taddr + sub * kColsPerWarp + h * 32, v[h]);
         }
         release(ok, buf);
 #pragma unroll
-        for (int h = 0; h < 2 && ok; ++h) {
-          const int c0 = sub * 64 + h * 32;
+        for (int h = 0; h < kChunks && ok; ++h) {
+          const int c0 = sub * kColsPerWarp + h * 32;
           __syncwarp();                         // the previous chunk's rows have been read
 #pragma unroll
           for (int j = 0; j < 32; j += 4)
@@ -620,10 +627,10 @@ cudaError_t prefill_prepare(moe_ctx* c) {
             make_tmap(&c->pf_tm[2], c->pf_xq, rows, d / 2, kBM) &&
             make_tmap(&c->pf_tm[3], c->pf_hq, rows, f / 2, kBM);
   if (!ok) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(moe_gemm_kernel<kStagesGateUp, 0, kBNGateUp>,
+  e = cudaFuncSetAttribute(moe_gemm_kernel<kStagesGateUp, 0, kBNGateUp, kEpiGateUp>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemGateUp);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(moe_gemm_kernel<kStagesDown, 1, kBNDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(moe_gemm_kernel<kStagesDown, 1, kBNDown, kEpiDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemDown);
 }
 
@@ -647,7 +654,7 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   g.K = d;
   g.hq_codes = c->pf_hq;
   g.hq_sf = c->pf_hsf;
-  moe_gemm_kernel<kStagesGateUp, 0, kBNGateUp>
+  moe_gemm_kernel<kStagesGateUp, 0, kBNGateUp, kEpiGateUp>
       <<<c->sm_count, PlanGateUp::threads, kSmemGateUp, s>>>(c->pf_tm[2], c->pf_tm[0], g);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // down projection -> per-slot outputs
@@ -657,7 +664,7 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   g.K = f;
   g.yacc = prefill_accumulates(c->cfg, T) ? c->yacc : nullptr;
   g.yexp = c->yexp;
-  moe_gemm_kernel<kStagesDown, 1, kBNDown>
+  moe_gemm_kernel<kStagesDown, 1, kBNDown, kEpiDown>
       <<<c->sm_count, PlanDown::threads, kSmemDown, s>>>(c->pf_tm[3], c->pf_tm[1], g);
   return cudaGetLastError();
 }
