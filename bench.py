@@ -223,6 +223,42 @@ def build_layers(lib, torch, synth, n_layers, max_tokens, bias=None, seed0=0):
     return ctxs
 
 
+def e2e_graph(torch, chunk, xh, yh, xd, yd, step, stream):
+    """One CUDA graph of `chunk` end-to-end steps, each with the host-to-device copy of its
+    input (pinned xh[i] -> device) and the device-to-host copy of its result (device -> pinned
+    yh[i]).  Two device buffers each way: step i's forward overlaps the input copy of step i+1
+    and the result copy of step i-1, which run on their own streams and are ordered by events
+    (a buffer is rewritten only after the forward or the copy that last read it)."""
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        fwd_done, out_done = [None, None], [None, None]
+        for i in range(chunk):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if fwd_done[b] is not None:
+                    s_in.wait_event(fwd_done[b])      # the forward of step i-2 has read xd[b]
+                xd[b].copy_(xh[i], non_blocking=True)
+                in_ready = torch.cuda.Event()
+                in_ready.record(s_in)
+            stream.wait_event(in_ready)
+            if out_done[b] is not None:
+                stream.wait_event(out_done[b])        # the result of step i-2 has left yd[b]
+            step(i, xd[b], yd[b])
+            fwd_done[b] = torch.cuda.Event()
+            fwd_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(fwd_done[b])
+                yh[i].copy_(yd[b], non_blocking=True)
+                out_done[b] = torch.cuda.Event()
+                out_done[b].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+    return g
+
+
 def run_ours(args):
     import torch
     import nvfp4_expert_ffn_gemv_b300 as lib
@@ -325,24 +361,23 @@ def run_ours(args):
     kern_ms = sorted(a.elapsed_time(b) for a, b in ev)
     ms = max_over_ranks(ms)
 
-    # end to end: pinned host tokens in, host result out, every step
+    # end to end: pinned host tokens in, host result out, every step (double-buffered)
     xh = x[:chunk].cpu().pin_memory()
     yh = torch.empty_like(xh).pin_memory()
-    xd = torch.empty((T, s.d_model), dtype=torch.bfloat16, device="cuda")
-    yd = torch.empty_like(xd)
-    ge = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(ge, stream=stream):
-        for i in range(chunk):
-            xd.copy_(xh[i], non_blocking=True)
-            if stack:
-                cur = xd
-                for l, c in enumerate(ctxs):
-                    out = yd if l == n_layers - 1 else bufs[l % 2]
-                    forward(c, cur, T, out, 1, stream)
-                    cur = out
-            else:
-                forward(ctxs[i % n_layers], xd, T, yd, 0, stream)
-            yh[i].copy_(yd, non_blocking=True)
+    xd = [torch.empty((T, s.d_model), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    yd = [torch.empty_like(xd[0]) for _ in range(2)]
+
+    def e2e_step(i, xdb, ydb):
+        if stack:
+            cur = xdb
+            for l, c in enumerate(ctxs):
+                out = ydb if l == n_layers - 1 else bufs[l % 2]
+                forward(c, cur, T, out, 1, stream)
+                cur = out
+        else:
+            forward(ctxs[i % n_layers], xdb, T, ydb, 0, stream)
+
+    ge = e2e_graph(torch, chunk, xh, yh, xd, yd, e2e_step, stream)
     with torch.cuda.stream(stream):
         ge.replay()
     torch.cuda.synchronize()
@@ -558,17 +593,12 @@ def run_dense(args):
     torch.cuda.synchronize()
     kern_ms = sorted(a.elapsed_time(b) for a, b in ev)
     ms = max_over_ranks(ms)
-    # end to end: pinned host token in, host result out, every step
+    # end to end: pinned host token in, host result out, every step (double-buffered)
     xh = x[:chunk].cpu().pin_memory()
     oh = torch.empty((chunk,) + tuple(out.shape[1:]), dtype=out.dtype).pin_memory()
-    xd = torch.empty_like(x[0])
-    od = torch.empty_like(out[0])
-    ge = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(ge, stream=stream):
-        for i in range(chunk):
-            xd.copy_(xh[i], non_blocking=True)
-            step(i, xd, od)
-            oh[i].copy_(od, non_blocking=True)
+    xd = [torch.empty_like(x[0]) for _ in range(2)]
+    od = [torch.empty_like(out[0]) for _ in range(2)]
+    ge = e2e_graph(torch, chunk, xh, oh, xd, od, step, stream)
     with torch.cuda.stream(stream):
         ge.replay()
     torch.cuda.synchronize()
