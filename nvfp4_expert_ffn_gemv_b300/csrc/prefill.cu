@@ -163,7 +163,7 @@ struct ActTables {
 // position blocks are not written: the GEMM rows are independent and the
 // outputs of padding rows are never read.
 constexpr int kMaxPerTok = 10;   // top_k (<= 8) + n_shared (<= 2)
-__global__ void __launch_bounds__(256, 3) quant_scatter_x_kernel(Routing r, const __nv_bfloat16* __restrict__ x, int T,
+__global__ void __launch_bounds__(256, 4) quant_scatter_x_kernel(Routing r, const __nv_bfloat16* __restrict__ x, int T,
                                                               int d, int k, int S, uint8_t* __restrict__ codes,
                                                               uint8_t* __restrict__ sf, float* __restrict__ yacc) {
   __shared__ int s_pos[kMaxActive], s_ppos[kMaxActive], s_prow[8][kMaxPerTok];
