@@ -3,7 +3,7 @@
     python nvfp4_expert_ffn_gemv_b300/microbench/run.py [name ...]
 
 Names: sync_burst_reduce, handoff, burst_issue, reduce_patterns, tma_stream, mma_rate,
-tmem_a_mma, mxf4_n256
+tmem_a_mma, mxf4_n256, splitf_tail
 (default: all).  Each prints its measurements; the summaries under profiles/
 quote them.  Binaries go to _build/microbench/.
 """
@@ -14,7 +14,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 OUT = os.path.join(os.path.dirname(os.path.dirname(HERE)), "_build", "microbench")
 NAMES = ("sync_burst_reduce", "handoff", "burst_issue", "reduce_patterns", "tma_stream", "mma_rate", "tmem_a_mma",
-         "mxf4_n256")
+         "mxf4_n256", "splitf_tail")
 
 
 def main(names):
