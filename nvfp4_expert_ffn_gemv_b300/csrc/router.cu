@@ -10,7 +10,8 @@
 //   router_partial: split-K GEMV/GEMM.  Block (kc, tile) multiplies a tile of TT
 //     tokens (8, or 32 from 256 tokens up) by the K-chunk kc of W_r [d][E];
 //     thread e owns expert e, so every W_r row is read as one coalesced 1 KB
-//     line and feeds TT FMAs.  Partial sums go to scratch.
+//     line and feeds TT FMAs; a thread's W_r loads of a chunk are all in
+//     flight together.  Partial sums go to scratch.
 //   router_topk: one CTA per token; thread e sums its nkc partials in a fixed
 //     order (deterministic) and adds the bias, then one warp runs k rounds of
 //     argmax over the (up to) 256 logits (8 per lane) and writes idx and the
@@ -47,11 +48,15 @@ __device__ __forceinline__ void stage_x_slab(const __nv_bfloat16* __restrict__ x
   }
 }
 
+// A thread requests WPRE rows of its W_r column before it uses any of them
+// (the first batch even before the x slab is staged, so the two latencies
+// overlap): a K chunk of up to WPRE rows costs one memory round trip.
 template <int TT>
 __global__ void __launch_bounds__(256) router_partial_kernel(
     const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, float* __restrict__ part,
     int T, int d, int E, int kc_len) {
   constexpr int XS = TT + 4;  // padded row of the transposed x slab
+  constexpr int WPRE = TT <= 8 ? 64 : 16;
   __shared__ __align__(16) float xs[kSlab][XS];
   const int kc = blockIdx.x;
   const int t0 = blockIdx.y * TT;
@@ -63,22 +68,32 @@ __global__ void __launch_bounds__(256) router_partial_kernel(
   const int kbeg = kc * kc_len;
   for (int k0 = kbeg; k0 < kbeg + kc_len; k0 += kSlab) {
     const int slab = min(kSlab, kbeg + kc_len - k0);
+    const float* wp = wr + (size_t)k0 * E + (e < E ? e : 0);
+    float wv[WPRE];
+#pragma unroll
+    for (int i = 0; i < WPRE; ++i) wv[i] = (e < E && i < slab) ? __ldg(wp + (size_t)i * E) : 0.f;
     __syncthreads();
     stage_x_slab<TT, 1>(x, d, t0, nt, k0, slab, &xs[0][0]);
     __syncthreads();
     if (e < E) {
-      const float* wp = wr + (size_t)k0 * E + e;
-#pragma unroll 4
-      for (int kk = 0; kk < slab; ++kk) {
-        const float wv = __ldg(wp + (size_t)kk * E);
-        const float4* xv = reinterpret_cast<const float4*>(&xs[kk][0]);
+      for (int kb = 0; kb < slab; kb += WPRE) {
+        if (kb > 0) {
 #pragma unroll
-        for (int q = 0; q < TT / 4; ++q) {
-          const float4 v = xv[q];
-          acc[4 * q + 0] = fmaf(v.x, wv, acc[4 * q + 0]);
-          acc[4 * q + 1] = fmaf(v.y, wv, acc[4 * q + 1]);
-          acc[4 * q + 2] = fmaf(v.z, wv, acc[4 * q + 2]);
-          acc[4 * q + 3] = fmaf(v.w, wv, acc[4 * q + 3]);
+          for (int i = 0; i < WPRE; ++i) wv[i] = kb + i < slab ? __ldg(wp + (size_t)(kb + i) * E) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < WPRE; ++i) {
+          if (kb + i < slab) {
+            const float4* xv = reinterpret_cast<const float4*>(&xs[kb + i][0]);
+#pragma unroll
+            for (int q = 0; q < TT / 4; ++q) {
+              const float4 v = xv[q];
+              acc[4 * q + 0] = fmaf(v.x, wv[i], acc[4 * q + 0]);
+              acc[4 * q + 1] = fmaf(v.y, wv[i], acc[4 * q + 1]);
+              acc[4 * q + 2] = fmaf(v.z, wv[i], acc[4 * q + 2]);
+              acc[4 * q + 3] = fmaf(v.w, wv[i], acc[4 * q + 3]);
+            }
+          }
         }
       }
     }
