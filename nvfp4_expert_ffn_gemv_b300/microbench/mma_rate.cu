@@ -18,6 +18,16 @@
 //   ... + TMEM reads       the same, while warps 1-3 keep reading the other
 //                          accumulator's columns (tcgen05.ld 32x32b.x32), as
 //                          the GEMM's epilogue does
+//   cp 128x256b / 128x128b the cost of the other tcgen05.cp shapes (no
+//                          multicast: 128 lanes x 32 or 16 bytes, 4 KB or 2 KB
+//                          into TMEM per copy) against 32x128b.warpx4 (512 B
+//                          read, written to all four lane quarters: 2 KB);
+//                          sources are arbitrary shared-memory bytes
+//   2 threads: ...         the scale copies issued by a second thread (warp 1)
+//                          into a 4-slot ring of TMEM scale columns: it
+//                          commits each stage's copies to an mbarrier that the
+//                          MMA thread waits on, and the MMA thread's commit
+//                          frees the slot again
 // Every CTA (one per SM) runs 256 stages; the time is from the first issue to
 // the completion of the last operation (tcgen05.commit), in SM cycles.
 // Operand values are arbitrary: only the rate is measured.
@@ -44,13 +54,24 @@ struct Variant {
   int pre;      // write all scale columns once before timing
   int stream;   // concurrent TMA stream into shared memory
   int tld;      // concurrent TMEM loads by warps 1-3
+  int split;    // scale copies issued by a second thread
+  int shape;    // copy shape: 0 = 32x128b.warpx4, 1 = 128x256b, 2 = 128x128b
 };
+
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
+
+constexpr int kSfSlots = 4, kSfSlotCols = 48;   // ring of scale columns at 256 .. 447
 
 __global__ void __launch_bounds__(128, 1) rate_kernel(Variant v, const uint8_t* __restrict__ src,
                                                       unsigned long long* cycles, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t done_bar, stage_bar, ring_bar[kSlots];
+  __shared__ __align__(8) uint64_t done_bar, stage_bar, ring_bar[kSlots], sf_full[kSfSlots], sf_empty[kSfSlots];
   __shared__ volatile int mma_done;
   __shared__ uint32_t tmem_base_s;
   for (int i = threadIdx.x; i < kUsed / 16; i += blockDim.x)
@@ -59,6 +80,10 @@ __global__ void __launch_bounds__(128, 1) rate_kernel(Variant v, const uint8_t* 
     mbar_init(&done_bar, 1);
     mbar_init(&stage_bar, 1);
     for (int k = 0; k < kSlots; ++k) mbar_init(&ring_bar[k], 1);
+    for (int k = 0; k < kSfSlots; ++k) {
+      mbar_init(&sf_full[k], 1);
+      mbar_init(&sf_empty[k], 1);
+    }
     mma_done = 0;
     fence_barrier_init();
   }
@@ -68,7 +93,46 @@ __global__ void __launch_bounds__(128, 1) rate_kernel(Variant v, const uint8_t* 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  if (threadIdx.x == 0) {
+  if (v.split) {
+    const uint32_t idesc = idesc_mxf4nvf4(128, v.n);
+    const uint64_t adesc = desc_kmajor_sw128(smem_u32(smem + kOffA));
+    const uint64_t bdesc = desc_kmajor_sw128(smem_u32(smem + kOffB));
+    if (threadIdx.x == 0) {
+      const unsigned long long t0 = clock64();
+      bool ok = true;
+      for (int s = 0; s < kStages && ok; ++s) {
+        const int slot = s % kSfSlots;
+        if (!wait_parity(&sf_full[slot], (uint32_t)(s / kSfSlots) & 1u)) { atomicExch(err, 4); ok = false; break; }
+        tc_fence_after();
+        const uint32_t base = tmem + 256 + slot * kSfSlotCols;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_mxf4nvf4(tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, base + kk * 4,
+                       base + 16 + kk * 8, s > 0 || kk > 0);
+        tc_commit(&sf_empty[slot]);
+      }
+      tc_commit(&done_bar);
+      ok = wait_parity(&done_bar, 0) && ok;
+      const unsigned long long t1 = clock64();
+      if (!ok) atomicExch(err, 1);
+      cycles[blockIdx.x] = t1 - t0;
+    } else if (threadIdx.x == 32) {
+      for (int s = 0; s < kStages; ++s) {
+        const int slot = s % kSfSlots;
+        if (!wait_parity(&sf_empty[slot], ((uint32_t)(s / kSfSlots) & 1u) ^ 1u)) { atomicExch(err, 5); break; }
+        tc_fence_after();
+        const uint32_t base = tmem + 256 + slot * kSfSlotCols;
+        for (int c = 0; c < v.ncp; ++c)
+          tmem_cp_sf_atom(base + 4 * c, desc_sf_atom(smem_u32(smem + kOffSF + 512 * c)));
+        tc_commit(&sf_full[slot]);
+      }
+      // the last stages' slots: wait until the MMA thread has consumed them
+      for (int s = kStages; s < kStages + kSfSlots; ++s) {
+        const int slot = s % kSfSlots;
+        if (!wait_parity(&sf_empty[slot], ((uint32_t)(s / kSfSlots) & 1u) ^ 1u)) { atomicExch(err, 6); break; }
+      }
+    }
+  } else if (threadIdx.x == 0) {
     const uint32_t idesc = idesc_mxf4nvf4(128, v.n > 0 ? v.n : 128);
     const uint64_t adesc = desc_kmajor_sw128(smem_u32(smem + kOffA));
     const uint64_t bdesc = desc_kmajor_sw128(smem_u32(smem + kOffB));
@@ -81,8 +145,18 @@ __global__ void __launch_bounds__(128, 1) rate_kernel(Variant v, const uint8_t* 
     }
     const unsigned long long t0 = clock64();
     for (int s = 0; s < kStages; ++s) {
-      for (int c = 0; c < v.ncp; ++c)
-        tmem_cp_sf_atom(tmem + 256 + 4 * c, desc_sf_atom(smem_u32(smem + kOffSF + 512 * c)));
+      if (v.shape == 1) {
+        // 128 rows x 32 bytes from the A region: 16 row groups of two 128-byte core matrices
+        for (int c = 0; c < v.ncp; ++c)
+          tmem_cp_128x256b(tmem + 256 + 8 * c, smem_desc(smem_u32(smem + kOffA), 128, 256, kLayoutNone));
+      } else if (v.shape == 2) {
+        // 128 rows x 16 bytes: 16 row groups of one 128-byte core matrix
+        for (int c = 0; c < v.ncp; ++c)
+          tmem_cp_128x128b(tmem + 256 + 4 * c, smem_desc(smem_u32(smem + kOffA), 128, 128, kLayoutNone));
+      } else {
+        for (int c = 0; c < v.ncp; ++c)
+          tmem_cp_sf_atom(tmem + 256 + 4 * c, desc_sf_atom(smem_u32(smem + kOffSF + 512 * c)));
+      }
       if (v.n > 0) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -161,15 +235,18 @@ int main() {
   const Variant vs[] = {{128, 0, 0, 0}, {256, 0, 0, 0}, {0, 8, 0, 0}, {128, 8, 0, 0}, {256, 12, 0, 0},
                         {128, 4, 0, 0}, {256, 8, 0, 0}, {128, 0, 1, 0}, {256, 0, 1, 0},
                         {128, 0, 1, 1}, {256, 0, 1, 1}, {128, 8, 0, 1}, {256, 12, 0, 1},
-                        {128, 0, 1, 0, 1}, {128, 8, 0, 0, 1}};
+                        {128, 0, 1, 0, 1}, {128, 8, 0, 0, 1}, {256, 12, 0, 0, 0, 1}, {128, 8, 0, 0, 0, 1},
+                        {0, 6, 0, 0, 0, 0, 1}, {0, 12, 0, 0, 0, 0, 2}, {256, 6, 0, 0, 0, 0, 1}};
   const char* names[] = {"mma N=128", "mma N=256", "cp x8", "cp x8 + mma N=128", "cp x12 + mma N=256",
                          "cp x4 + mma N=128", "cp x8 + mma N=256", "(valid scales) mma N=128",
                          "(valid scales) mma N=256", "mma N=128 + TMA stream", "mma N=256 + TMA stream",
                          "cp x8 + mma N=128 + TMA", "cp x12 + mma N=256 + TMA", "mma N=128 + TMEM reads",
-                         "cp x8 + mma N=128 + TMEM reads"};
+                         "cp x8 + mma N=128 + TMEM reads", "2 threads: cp x12 + mma N=256",
+                         "2 threads: cp x8 + mma N=128", "cp 128x256b x6", "cp 128x128b x12",
+                         "cp 128x256b x6 + mma N=256"};
   unsigned long long h[1024];
   if (nsm > 1024) return 1;
-  for (int i = 0; i < 15; ++i) {
+  for (int i = 0; i < 20; ++i) {
     rate_kernel<<<nsm, 128, kSmem>>>(vs[i], src, cyc, err);   // warm-up
     CK(cudaGetLastError());
     rate_kernel<<<nsm, 128, kSmem>>>(vs[i], src, cyc, err);
