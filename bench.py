@@ -56,9 +56,9 @@ FP4_OVER_BF16 = 13.5 / 2.25                                          # nominal d
 HBM_NOMINAL_GBS = 8000.0                                             # the ~8 TB/s the targets are quoted against
 
 WORKLOADS = {
-    "decode_b1": dict(T=1, layers=16, steps=50000, chunk=1000,
+    "decode_b1": dict(T=1, layers=16, steps=50000, chunk=1000, e2e_depth=8,
                       metric="MoE decode tok/s (batch-1, one Flint-shaped NVFP4 MoE layer)"),
-    "decode_b64": dict(T=64, layers=16, steps=2000, chunk=100,
+    "decode_b64": dict(T=64, layers=16, steps=2000, chunk=100, e2e_depth=8,
                        metric="MoE decode tok/s (batch-64 Zipf-skewed, one Flint-shaped NVFP4 MoE layer)"),
     "stack": dict(T=1, layers=N_LAYERS_STACK, steps=512, chunk=1,
                   metric="MoE decode tok/s (batch-1, 47-layer Flint MoE stack, attention omitted)"),
@@ -66,9 +66,9 @@ WORKLOADS = {
                     metric="MoE prefill tok/s (4096 tokens, one Flint-shaped NVFP4 MoE layer)"),
     "prefill_32k": dict(T=32768, layers=4, steps=8, chunk=2,
                         metric="MoE prefill tok/s (32768 tokens, one Flint-shaped NVFP4 MoE layer)"),
-    "lm_head": dict(T=1, layers=2, steps=2000, chunk=200,
+    "lm_head": dict(T=1, layers=2, steps=2000, chunk=200, e2e_depth=8,
                     metric="lm_head decode tok/s (batch-1, 151936 x 2048 NVFP4 output layer)"),
-    "dense_ffn": dict(T=1, layers=4, steps=4000, chunk=400,
+    "dense_ffn": dict(T=1, layers=4, steps=4000, chunk=400, e2e_depth=8,
                       metric="dense FFN decode tok/s (batch-1, 2048 x 18432 NVFP4 SwiGLU layer)"),
 }
 DENSE_WORKLOADS = ("lm_head", "dense_ffn")
@@ -223,37 +223,48 @@ def build_layers(lib, torch, synth, n_layers, max_tokens, bias=None, seed0=0):
     return ctxs
 
 
-def e2e_graph(torch, chunk, xh, yh, xd, yd, step, stream):
-    """One CUDA graph of `chunk` end-to-end steps, each with the host-to-device copy of its
-    input (pinned xh[i] -> device) and the device-to-host copy of its result (device -> pinned
-    yh[i]).  Two device buffers each way: step i's forward overlaps the input copy of step i+1
-    and the result copy of step i-1, which run on their own streams and are ordered by events
-    (a buffer is rewritten only after the forward or the copy that last read it)."""
+def e2e_graph(torch, chunk, xh, yh, xd, yd, step, stream, depth=1):
+    """One CUDA graph of `chunk` end-to-end steps.  Every step has its own host-to-device copy of
+    its input (pinned xh[i] -> device) and its own device-to-host copy of its result (device ->
+    pinned yh[i]), on two side streams.  The steps run in blocks of `depth`: a block's input copies
+    are issued together once their buffers are free (the forwards of two blocks back have read
+    them), and the block's first forward waits for them and for the result copies of two blocks
+    back (whose buffers it rewrites).  Inside a block no other edge enters the forward stream, so
+    consecutive steps keep their programmatic (PDL) overlap: a cross-stream wait in front of a
+    forward costs it that overlap, while the result copies, which only leave the stream, do not.
+    xd / yd hold 2 * depth device buffers each."""
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    nb = 2 * depth
+    assert len(xd) >= nb and len(yd) >= nb
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         s_in.wait_stream(stream)
         s_out.wait_stream(stream)
-        fwd_done, out_done = [None, None], [None, None]
-        for i in range(chunk):
-            b = i % 2
+        fwd_done, out_done = {}, {}               # block -> its last forward / its result copies
+        for j0 in range(0, chunk, depth):
+            j = j0 // depth
+            steps = range(j0, min(chunk, j0 + depth))
             with torch.cuda.stream(s_in):
-                if fwd_done[b] is not None:
-                    s_in.wait_event(fwd_done[b])      # the forward of step i-2 has read xd[b]
-                xd[b].copy_(xh[i], non_blocking=True)
+                if j - 2 in fwd_done:
+                    s_in.wait_event(fwd_done[j - 2])
+                for i in steps:
+                    xd[i % nb].copy_(xh[i], non_blocking=True)
                 in_ready = torch.cuda.Event()
                 in_ready.record(s_in)
             stream.wait_event(in_ready)
-            if out_done[b] is not None:
-                stream.wait_event(out_done[b])        # the result of step i-2 has left yd[b]
-            step(i, xd[b], yd[b])
-            fwd_done[b] = torch.cuda.Event()
-            fwd_done[b].record(stream)
+            if j - 2 in out_done:
+                stream.wait_event(out_done[j - 2])
+            for i in steps:
+                step(i, xd[i % nb], yd[i % nb])
+                done = torch.cuda.Event()
+                done.record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done)
+                    yh[i].copy_(yd[i % nb], non_blocking=True)
+            fwd_done[j] = done
             with torch.cuda.stream(s_out):
-                s_out.wait_event(fwd_done[b])
-                yh[i].copy_(yd[b], non_blocking=True)
-                out_done[b] = torch.cuda.Event()
-                out_done[b].record(s_out)
+                out_done[j] = torch.cuda.Event()
+                out_done[j].record(s_out)
         stream.wait_stream(s_in)
         stream.wait_stream(s_out)
     return g
@@ -364,8 +375,9 @@ def run_ours(args):
     # end to end: pinned host tokens in, host result out, every step (double-buffered)
     xh = x[:chunk].cpu().pin_memory()
     yh = torch.empty_like(xh).pin_memory()
-    xd = [torch.empty((T, s.d_model), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
-    yd = [torch.empty_like(xd[0]) for _ in range(2)]
+    depth = min(wl.get("e2e_depth", 1), chunk)
+    xd = [torch.empty((T, s.d_model), dtype=torch.bfloat16, device="cuda") for _ in range(2 * depth)]
+    yd = [torch.empty_like(xd[0]) for _ in range(2 * depth)]
 
     def e2e_step(i, xdb, ydb):
         if stack:
@@ -377,12 +389,16 @@ def run_ours(args):
         else:
             forward(ctxs[i % n_layers], xdb, T, ydb, 0, stream)
 
-    ge = e2e_graph(torch, chunk, xh, yh, xd, yd, e2e_step, stream)
+    ge = e2e_graph(torch, chunk, xh, yh, xd, yd, e2e_step, stream, depth)
     with torch.cuda.stream(stream):
         ge.replay()
     torch.cuda.synchronize()
     e2e_ms = timed(ge, replays)
     e2e_ms = max_over_ranks(e2e_ms)
+    if not prefill:
+        # the decode kernels are deterministic: the host results equal the device-resident run's
+        if not torch.equal(yh, y[:chunk].cpu()):
+            raise RuntimeError("end-to-end results differ from the device-resident run")
 
     # algorithmic bytes of a batched-decode step: every distinct chosen expert once, plus the shared one
     # expert load of the timed inputs (routing only, outside the timed region): distinct experts
@@ -487,7 +503,8 @@ def run_ours(args):
     if load is not None:
         line["expert_load"] = load
     line["e2e"] = {"value": round(tok / (e2e_ms / 1e3), 1), "unit": "tok/s",
-                   "h2d_bytes_per_step": T * D_MODEL * 2, "d2h_bytes_per_step": T * D_MODEL * 2}
+                   "h2d_bytes_per_step": T * D_MODEL * 2, "d2h_bytes_per_step": T * D_MODEL * 2,
+                   "input_copies_ahead": depth}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
@@ -596,9 +613,10 @@ def run_dense(args):
     # end to end: pinned host token in, host result out, every step (double-buffered)
     xh = x[:chunk].cpu().pin_memory()
     oh = torch.empty((chunk,) + tuple(out.shape[1:]), dtype=out.dtype).pin_memory()
-    xd = [torch.empty_like(x[0]) for _ in range(2)]
-    od = [torch.empty_like(out[0]) for _ in range(2)]
-    ge = e2e_graph(torch, chunk, xh, oh, xd, od, step, stream)
+    depth = min(wl.get("e2e_depth", 1), chunk)
+    xd = [torch.empty_like(x[0]) for _ in range(2 * depth)]
+    od = [torch.empty_like(out[0]) for _ in range(2 * depth)]
+    ge = e2e_graph(torch, chunk, xh, oh, xd, od, step, stream, depth)
     with torch.cuda.stream(stream):
         ge.replay()
     torch.cuda.synchronize()
@@ -631,7 +649,7 @@ def run_dense(args):
                      "algorithmic_bytes_per_launch": alg, "traffic": _traffic(args.workload),
                      "launch_us": round(step_ms * 1e3, 3), "launch_us_isolated": kus},
         "e2e": {"value": round(tok / (e2e_ms / 1e3), 1), "unit": "tok/s", "h2d_bytes_per_step": T * d * 2,
-                "d2h_bytes_per_step": T * (V * 4 if head else d * 2)},
+                "d2h_bytes_per_step": T * (V * 4 if head else d * 2), "input_copies_ahead": depth},
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
