@@ -28,6 +28,13 @@
 // gate rows + the matching 8 up rows) applies SwiGLU in registers and writes
 // h (fp32); the dense down pass writes fp32 partial sums per K slice, which a
 // small kernel adds in a fixed order (plus the residual) into bf16 y.
+//
+// Every kernel of a forward is launched with programmatic dependent launch
+// (PDL): it may start while its predecessor in the stream is still running,
+// and waits for it (griddepcontrol.wait) before it touches anything the
+// predecessor writes.  The GEMV's weight stream does not depend on earlier
+// kernels, so its producer warp starts filling the stage ring at once, while
+// the small kernel before it (the activation prescale) still runs.
 #include "internal.h"
 #include "mma_frag.cuh"
 #include "sm100.cuh"
@@ -65,6 +72,24 @@ struct GemvArgs {
 };
 
 __device__ __forceinline__ uint2 ldg64(const uint8_t* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // Stage layout of one unit: the 16 code rows (KS/2 bytes each, a multiple of
 // 128) and then the 16 scale rows (KS/16 bytes each), as one bulk copy each.
@@ -238,6 +263,7 @@ __global__ void __launch_bounds__(32 * (2 * kMaxStages + 1), 1) nvfp4_gemv_kerne
   const uint32_t rcodes = (uint32_t)g.KS / 2, rscales = (uint32_t)g.KS / 16;     // bytes per row
   const uint32_t stage_bytes = stage_bytes_of(g.KS), scale_off = 16 * rcodes;
   const int units = g.ntiles * g.nslices;
+  griddep_launch();
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -248,6 +274,7 @@ __global__ void __launch_bounds__(32 * (2 * kMaxStages + 1), 1) nvfp4_gemv_kerne
   __syncthreads();
   bool ok = true;
   if (warp == 0) {
+    // the weights were written at init: no wait on the previous kernel
     if (lane == 0) {
       int j = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
@@ -264,7 +291,9 @@ __global__ void __launch_bounds__(32 * (2 * kMaxStages + 1), 1) nvfp4_gemv_kerne
     // every copy issued here lands before the consumer that owns its stage
     // finishes, and the CTA leaves only after all consumers (below)
   } else if (warp - 1 < 2 * NS) {
-    // warps 2s + 1 and 2s + 2 share stage s, each on one half of the K slice
+    // warps 2s + 1 and 2s + 2 share stage s, each on one half of the K slice;
+    // the activations and every output buffer belong to the previous kernels
+    griddep_wait();
     const int s = (warp - 1) >> 1, half = (warp - 1) & 1;
     int j = s;
     for (int u = blockIdx.x + s * gridDim.x; u < units; u += NS * gridDim.x, j += NS) {
@@ -309,6 +338,8 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* __rest
                                                      uint8_t* __restrict__ out, float* __restrict__ unshift,
                                                      uint32_t* __restrict__ hmax) {
   __shared__ uint32_t red[8];
+  griddep_launch();
+  griddep_wait();
   const int t = blockIdx.x;
   if (hmax && threadIdx.x == 0) hmax[t] = 0u;   // the dense FFN's gate/up pass folds max |h| in here
   uint8_t* dst = out + (size_t)t * K * 2;
@@ -353,6 +384,8 @@ constexpr int kPrepHChunk = 2048;
 __global__ void __launch_bounds__(256) prep_h_kernel(const float* __restrict__ h, int T, int K,
                                                      const uint32_t* __restrict__ hmax, uint8_t* __restrict__ hi,
                                                      uint8_t* __restrict__ lo, float* __restrict__ unshift) {
+  griddep_launch();
+  griddep_wait();
   const int t = blockIdx.y;
   const int i0 = blockIdx.x * (kPrepHChunk / 4), i1 = min(K / 4, i0 + kPrepHChunk / 4);
   uint8_t* dh = hi + (size_t)t * K * 2;
@@ -386,6 +419,8 @@ __global__ void __launch_bounds__(256) prep_h_kernel(const float* __restrict__ h
 __global__ void __launch_bounds__(256) reduce_down_kernel(const float* __restrict__ part, int S, int T, int d,
                                                           const __nv_bfloat16* __restrict__ x, int residual,
                                                           __nv_bfloat16* __restrict__ y) {
+  griddep_launch();
+  griddep_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= T * d) return;
   float acc = 0.f;
@@ -444,8 +479,7 @@ cudaError_t launch_gemv(GemvArgs g, int sm_count, cudaStream_t s) {
   const int units = g.ntiles * g.nslices;
   const int grid = units < sm_count ? units : sm_count;
   g.nstages = stages_for(g.KS);
-  nvfp4_gemv_kernel<MODE><<<grid, 32 * (2 * g.nstages + 1), gemv_smem(g.KS), s>>>(g);
-  return cudaGetLastError();
+  return launch_pdl(nvfp4_gemv_kernel<MODE>, dim3(grid), dim3(32 * (2 * g.nstages + 1)), gemv_smem(g.KS), s, g);
 }
 
 }  // namespace
@@ -619,8 +653,9 @@ moe_status moe_head_forward(moe_dense* x, const void* x_bf16, int T, float* logi
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x_bf16);
   for (int t0 = 0; t0 < T; t0 += kTokPass) {
     const int n = T - t0 < kTokPass ? T - t0 : kTokPass;
-    prep_x_kernel<<<rows_read(n), 256, 0, s>>>(xb + (size_t)t0 * x->d, n, x->d, x->x16, x->xun, nullptr);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_pdl(prep_x_kernel, dim3(rows_read(n)), dim3(256), 0, s, xb + (size_t)t0 * x->d, n, x->d, x->x16,
+                   x->xun, (uint32_t*)nullptr) != cudaSuccess)
+      return MOE_ERR_CUDA;
     GemvArgs g = base_args(x, n);
     g.codes = x->codes;
     g.scales = x->scales;
@@ -725,8 +760,9 @@ moe_status moe_ffn_forward(moe_dense* x, const void* x_bf16, int T, void* y_bf16
   const int d = x->d, f = x->f;
   for (int t0 = 0; t0 < T; t0 += kTokPass) {
     const int n = T - t0 < kTokPass ? T - t0 : kTokPass;
-    prep_x_kernel<<<rows_read(n), 256, 0, s>>>(xb + (size_t)t0 * d, n, d, x->x16, x->xun, x->hmax);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_pdl(prep_x_kernel, dim3(rows_read(n)), dim3(256), 0, s, xb + (size_t)t0 * d, n, d, x->x16, x->xun,
+                   x->hmax) != cudaSuccess)
+      return MOE_ERR_CUDA;
     GemvArgs g = base_args(x, n);
     g.codes = x->codes;
     g.scales = x->scales;
@@ -741,9 +777,10 @@ moe_status moe_ffn_forward(moe_dense* x, const void* x_bf16, int T, void* y_bf16
     g.out_ld = f;
     g.hmax = x->hmax;
     if (launch_gemv<kModeGateUp>(g, x->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
-    prep_h_kernel<<<dim3((unsigned)((f + kPrepHChunk - 1) / kPrepHChunk), (unsigned)rows_read(n)), 256, 0, s>>>(
-        x->h, n, f, x->hmax, x->h_hi, x->h_lo, x->hun);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_pdl(prep_h_kernel, dim3((unsigned)((f + kPrepHChunk - 1) / kPrepHChunk), (unsigned)rows_read(n)),
+                   dim3(256), 0, s, (const float*)x->h, n, f, (const uint32_t*)x->hmax, x->h_hi, x->h_lo,
+                   x->hun) != cudaSuccess)
+      return MOE_ERR_CUDA;
     GemvArgs dn = base_args(x, n);
     dn.codes = x->dn_codes;
     dn.scales = x->dn_scales;
@@ -760,9 +797,9 @@ moe_status moe_ffn_forward(moe_dense* x, const void* x_bf16, int T, void* y_bf16
     dn.out = x->part;
     dn.out_ld = d;
     if (launch_gemv<kModeDown>(dn, x->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
-    reduce_down_kernel<<<(n * d + 255) / 256, 256, 0, s>>>(x->part, x->S, n, d, xb + (size_t)t0 * d, residual,
-                                                         yb + (size_t)t0 * d);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_pdl(reduce_down_kernel, dim3((n * d + 255) / 256), dim3(256), 0, s, (const float*)x->part, x->S, n,
+                   d, xb + (size_t)t0 * d, residual, yb + (size_t)t0 * d) != cudaSuccess)
+      return MOE_ERR_CUDA;
   }
   return MOE_OK;
 }
