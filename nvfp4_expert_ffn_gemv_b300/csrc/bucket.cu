@@ -17,6 +17,7 @@
 // otherwise they go through global scratch.  From 1024 tokens on, the same
 // phases run as three grids (see below), so A and D use every SM.
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace nvmoe {
 
@@ -127,6 +128,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T
   const int nchunks = (T + 31) / 32;
   uint8_t* ej_s = bsm + (size_t)nchunks * E * 2;
   uint8_t* rank_s = ej_s + (size_t)T * k;
+  pdl_trigger();
+  pdl_wait();
 
   // A. per-chunk ranks and counts
   for (int c = warp; c < nchunks; c += nwarps) {
@@ -236,6 +239,8 @@ constexpr int kScanBatch = 32;                       // loads in flight per thre
 __global__ void __launch_bounds__(kGroupChunks * 32) bucket_count_kernel(Routing r, int T, int k, int E,
                                                                          int* status) {
   __shared__ uint32_t mask[kGroupChunks][kMaxE];
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = (T + 31) / 32;
   const int g = blockIdx.x, c = g * kGroupChunks + warp;
@@ -278,6 +283,8 @@ __global__ void __launch_bounds__(kScanThreads) bucket_scan_kernel(Routing r, in
   __shared__ int part[kScanParts][kMaxE];
   __shared__ int cnt[kMaxE];
   __shared__ int off[kMaxE + 1];
+  pdl_trigger();
+  pdl_wait();
   const int e = threadIdx.x % kMaxE, q = threadIdx.x / kMaxE;
   const int ngroups = ((T + 31) / 32 + kGroupChunks - 1) / kGroupChunks;
   const int per = (ngroups + kScanParts - 1) / kScanParts;
@@ -316,6 +323,8 @@ __global__ void __launch_bounds__(kScanThreads) bucket_scan_kernel(Routing r, in
 }
 
 __global__ void __launch_bounds__(256) bucket_scatter_kernel(Routing r, int T, int k, int E, int S) {
+  pdl_trigger();
+  pdl_wait();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s < T * k) {
     const int t = s / k;
@@ -352,18 +361,19 @@ cudaError_t launch_bucket(const moe_ctx* c, int T, cudaStream_t s) {
   const int k = c->cfg.top_k, E = c->cfg.n_experts, S = c->cfg.n_shared;
   if (T >= kBucketGridTokens) {
     const int ngroups = (T + 32 * kGroupChunks - 1) / (32 * kGroupChunks);
-    bucket_count_kernel<<<ngroups, kGroupChunks * 32, 0, s>>>(c->r, T, k, E, c->status);
-    bucket_scan_kernel<<<1, kScanThreads, 0, s>>>(c->r, T, k, E, S, c->status);
+    cudaError_t e = launch_maybe_pdl(use_pdl(T), bucket_count_kernel, dim3(ngroups), dim3(kGroupChunks * 32), 0, s, c->r, T, k,
+                                    E, c->status);
+    if (e == cudaSuccess)
+      e = launch_maybe_pdl(use_pdl(T), bucket_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, c->r, T, k, E, S, c->status);
     const int n = T * k + S * T;
-    bucket_scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(c->r, T, k, E, S);
-    return cudaGetLastError();
+    if (e == cudaSuccess)
+      e = launch_maybe_pdl(use_pdl(T), bucket_scatter_kernel, dim3((n + 255) / 256), dim3(256), 0, s, c->r, T, k, E, S);
+    return e;
   }
   const size_t smem = bucket_smem_bytes(T, k, E);
   if (smem <= kBucketSmemMax)
-    bucket_kernel<true><<<1, kBucketThreads, smem, s>>>(c->r, T, k, E, S, c->status);
-  else
-    bucket_kernel<false><<<1, kBucketThreads, 0, s>>>(c->r, T, k, E, S, c->status);
-  return cudaGetLastError();
+    return launch_maybe_pdl(use_pdl(T), bucket_kernel<true>, dim3(1), dim3(kBucketThreads), smem, s, c->r, T, k, E, S, c->status);
+  return launch_maybe_pdl(use_pdl(T), bucket_kernel<false>, dim3(1), dim3(kBucketThreads), 0, s, c->r, T, k, E, S, c->status);
 }
 
 }  // namespace nvmoe

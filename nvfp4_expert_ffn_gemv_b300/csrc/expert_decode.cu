@@ -16,6 +16,7 @@
 // weight rows;  down unit = (active expert, 64 output rows).  Each unit loops
 // over the expert's tokens in groups of kTG.
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace nvmoe {
 
@@ -353,6 +354,8 @@ __global__ void __launch_bounds__(256) combine_kernel(Routing r, const float* __
                                                       const __nv_bfloat16* __restrict__ x,
                                                       __nv_bfloat16* __restrict__ y, int T, int d,
                                                       int k, int S, int residual) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   int pos[8];
   float w[8];
@@ -395,9 +398,8 @@ __global__ void __launch_bounds__(256) combine_kernel(Routing r, const float* __
 
 cudaError_t launch_combine(const moe_ctx* c, const __nv_bfloat16* x, int T, __nv_bfloat16* y,
                            int residual, cudaStream_t s) {
-  combine_kernel<<<T, 256, 0, s>>>(c->r, c->yexp, x, y, T, c->cfg.d_model, c->cfg.top_k,
-                                   c->cfg.n_shared, residual);
-  return cudaGetLastError();
+  return launch_maybe_pdl(use_pdl(T), combine_kernel, dim3(T), dim3(256), 0, s, c->r, (const float*)c->yexp, x, y, T,
+                         c->cfg.d_model, c->cfg.top_k, c->cfg.n_shared, residual);
 }
 
 }  // namespace nvmoe

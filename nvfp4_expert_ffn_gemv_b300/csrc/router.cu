@@ -19,6 +19,7 @@
 #include <atomic>
 
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace nvmoe {
 
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(256) router_partial_kernel(
   const int t0 = blockIdx.y * TT;
   const int e = threadIdx.x;
   const int nt = min(TT, T - t0);
+  pdl_trigger();
   float acc[TT];
 #pragma unroll
   for (int t = 0; t < TT; ++t) acc[t] = 0.f;
@@ -72,6 +74,7 @@ __global__ void __launch_bounds__(256) router_partial_kernel(
     float wv[WPRE];
 #pragma unroll
     for (int i = 0; i < WPRE; ++i) wv[i] = (e < E && i < slab) ? __ldg(wp + (size_t)i * E) : 0.f;
+    if (k0 == kbeg) pdl_wait();   // the first W_r rows are on their way while the previous kernel ends
     __syncthreads();
     stage_x_slab<TT, 1>(x, d, t0, nt, k0, slab, &xs[0][0]);
     __syncthreads();
@@ -156,7 +159,9 @@ __global__ void __launch_bounds__(kStagedThreads, 1) router_partial_staged_kerne
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int s = 0; s < kWStages - 1; ++s) issue(s);
+  pdl_trigger();
+  for (int s = 0; s < kWStages - 1; ++s) issue(s);   // W_r only: before the wait
+  pdl_wait();
   for (int sub = 0; sub < nsub; ++sub) {
     __syncthreads();  // compute(sub - 1) is done: its W stage and (on a slab edge) xs are free
     const int kin = (sub * kWRows) % kSlab;
@@ -266,6 +271,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
     const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
     int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status, float* logits_out) {
   __shared__ float lg[256];
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const int e = threadIdx.x;
   if (e < E) {
@@ -298,6 +305,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
 __global__ void __launch_bounds__(256) router_topk_warp_kernel(
     const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
     int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status, float* logits_out) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -330,11 +339,10 @@ int router_tile(int T) { return T >= 256 ? 32 : 8; }
 cudaError_t launch_router_topk(const float* part, const float* bias, int has_bias, int T, int E, int K, int nkc,
                                int32_t* idx, float* w, int* status, float* logits_out, cudaStream_t s) {
   if (nkc <= 4)
-    router_topk_warp_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status,
-                                                         logits_out);
-  else
-    router_topk_kernel<<<T, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status, logits_out);
-  return cudaGetLastError();
+    return launch_maybe_pdl(use_pdl(T), router_topk_warp_kernel, dim3((T + 7) / 8), dim3(256), 0, s, part, bias, has_bias, T, E,
+                           K, nkc, idx, w, status, logits_out);
+  return launch_maybe_pdl(use_pdl(T), router_topk_kernel, dim3(T), dim3(256), 0, s, part, bias, has_bias, T, E, K, nkc, idx, w,
+                         status, logits_out);
 }
 
 namespace {
@@ -346,13 +354,14 @@ cudaError_t launch_router_kernels(const __nv_bfloat16* x, int T, const float* wr
   const int tt = router_tile(T);
   const dim3 g1(nkc, (T + tt - 1) / tt);
   const bool staged = E % 4 == 0 && (reinterpret_cast<uintptr_t>(wr) & 15u) == 0 && (d / nkc) % kWRows == 0;
+  cudaError_t err;
   if (tt == 32 && staged)
-    router_partial_staged_kernel<<<g1, kStagedThreads, staged_smem_bytes(), s>>>(x, wr, part, T, d, E, d / nkc);
+    err = launch_maybe_pdl(use_pdl(T), router_partial_staged_kernel, g1, dim3(kStagedThreads), staged_smem_bytes(), s, x, wr, part,
+                          T, d, E, d / nkc);
   else if (tt == 32)
-    router_partial_kernel<32><<<g1, 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
+    err = launch_maybe_pdl(use_pdl(T), router_partial_kernel<32>, g1, dim3(256), 0, s, x, wr, part, T, d, E, d / nkc);
   else
-    router_partial_kernel<8><<<g1, 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
-  cudaError_t err = cudaGetLastError();
+    err = launch_maybe_pdl(use_pdl(T), router_partial_kernel<8>, g1, dim3(256), 0, s, x, wr, part, T, d, E, d / nkc);
   if (err != cudaSuccess) return err;
   return launch_router_topk(part, bias, has_bias, T, E, K, nkc, idx, w, status, logits_out, s);
 }
