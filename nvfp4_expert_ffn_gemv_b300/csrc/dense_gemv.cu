@@ -69,6 +69,7 @@ struct GemvArgs {
   int nstages;             // stages = consumer warps
   int* status;
   int dbg;
+  const __nv_bfloat16* x1; // head at one token: the token's bf16 row (x in registers, FMA dot products)
 };
 
 __device__ __forceinline__ uint2 ldg64(const uint8_t* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
@@ -252,6 +253,140 @@ __device__ __forceinline__ void consume_unit(const GemvArgs& g, const uint8_t* s
   }
 }
 
+// One token through the output layer.  The MMA path would use one of the
+// eight B columns of every m16n8k16, so here each warp of the stage's pair
+// takes 8 of the unit's 16 rows whole: lane l holds the token's x for the
+// 32-column chunks j = l + 32q (exact f16 after its power-of-two prescale, as
+// the MMA path's B operand) and forms each row's partial dot with the
+// mixed-precision FMA (E2M1 code as exact f16 x f16 x + fp32; the block scale
+// applied once per 16 products).  The 8 row partials are summed over the
+// warp with a transposing reduction (9 shuffles), then lane 4r writes row r.
+__device__ __forceinline__ void fma2_mixed(uint32_t a, uint32_t b, float& acc, float& acc2) {
+  asm("{\n\t.reg .f16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %1, ah, bh, %1;\n\t}"
+      : "+f"(acc), "+f"(acc2) : "r"(a), "r"(b));
+}
+
+template <int CPL>
+__device__ __forceinline__ void load_x1(const GemvArgs& g, uint32_t (&xh)[CPL][16]) {
+  const int lane = threadIdx.x & 31;
+  const float sc = 1.f / g.unshift[0];   // a power of two
+#pragma unroll
+  for (int q = 0; q < CPL; ++q) {
+    const uint4* src = reinterpret_cast<const uint4*>(g.x1 + (size_t)(lane + 32 * q) * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = __ldg(src + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const __half2 hh = __floats2half2_rn(__uint_as_float(w[p] << 16) * sc, __uint_as_float(w[p] & 0xFFFF0000u) * sc);
+        xh[q][4 * i + p] = *reinterpret_cast<const uint32_t*>(&hh);
+      }
+    }
+  }
+}
+
+template <int CPL>
+__device__ __forceinline__ void consume_unit_t1(const GemvArgs& g, const uint8_t* sc, const uint8_t* ss, int tile,
+                                                int half, const uint32_t (&xh)[CPL][16], int bar_id) {
+  const int lane = threadIdx.x & 31;
+  const int CB = g.KS / 2, SB = g.KS / 16;
+  const bool sswz = (SB & 127) == 0;
+  float v[8];
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr) {
+    const int r = half * 8 + rr;
+    const uint8_t* crow = sc + r * CB;
+    const uint8_t* srow = ss + r * SB;
+    float dot = 0.f;
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+      const int j = lane + 32 * q;
+      const uint4 cw = *reinterpret_cast<const uint4*>(crow + swz(j * 16, r & 7));
+      const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
+      float b[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t o[4];
+        cvt_e2m1x8(ws[w], o);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) fma2_mixed(o[p], xh[q][4 * w + p], b[w >> 1][0], b[w >> 1][1]);
+      }
+      const int sb = sswz ? swz(2 * j, r & 7) : 2 * j;
+      const float2 s01 = e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t*>(srow + sb));
+      dot = fmaf(b[0][0] + b[0][1], s01.x, dot);
+      dot = fmaf(b[1][0] + b[1][1], s01.y, dot);
+    }
+    v[rr] = dot;
+  }
+  // transposing sum over the warp: after the xor-16, -8 and -4 steps lane l
+  // holds a partial of row (l >> 2) & 7, completed by the xor-2 and -1 steps
+  const int b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+  float w4[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b4 ? v[i + 4] : v[i], send = b4 ? v[i] : v[i + 4];
+    w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+  float w2[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b3 ? w4[i + 2] : w4[i], send = b3 ? w4[i] : w4[i + 2];
+    w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float t = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+  t += __shfl_xor_sync(0xffffffffu, t, 2);
+  t += __shfl_xor_sync(0xffffffffu, t, 1);
+  if ((lane & 3) == 0) g.out[tile * 16 + half * 8 + (lane >> 2)] = t * g.ts0 * g.unshift[0];
+  // both warps of the pair are done with the stage before the first one releases it
+  asm volatile("bar.sync %0, 64;" :: "r"(bar_id) : "memory");
+}
+
+// The consumer loops of stage s (warps 2s + 1 and 2s + 2, one per half).  Both
+// warps of the pair take the same path (the wait outcome is shared through the
+// barrier count only when both run): a failed wait skips nothing but is reported.
+template <int MODE>
+__device__ __forceinline__ bool consume_loop(const GemvArgs& g, const uint8_t* gsm, uint32_t stage_bytes,
+                                          uint32_t scale_off, uint64_t* full_bar, uint64_t* empty_bar,
+                                          float (*xch_all)[2][16 * 32], int s, int half, int units) {
+  const int lane = threadIdx.x & 31, NS = g.nstages;
+  bool ok = true;
+  int j = s;
+  for (int u = blockIdx.x + s * gridDim.x; u < units; u += NS * gridDim.x, j += NS) {
+    if (!wait_parity(&full_bar[s], (j / NS) & 1)) ok = false;
+    const uint8_t* sc = gsm + (size_t)s * stage_bytes;
+    const int slice = u / g.ntiles, tile = u % g.ntiles;
+    const int ngroups = (g.T + 7) / 8;
+    float* xch = xch_all[s][(j / NS) & 1];
+    if (ngroups <= 1) consume_unit<MODE, 1>(g, sc, sc + scale_off, slice, tile, half, xch, s + 1);
+    else if (ngroups == 2) consume_unit<MODE, 2>(g, sc, sc + scale_off, slice, tile, half, xch, s + 1);
+    else consume_unit<MODE, 4>(g, sc, sc + scale_off, slice, tile, half, xch, s + 1);
+    __syncwarp();
+    if (lane == 0 && half == 0) mbar_arrive(&empty_bar[s]);
+  }
+  return ok;
+}
+
+template <int CPL>
+__device__ __noinline__ bool consume_loop_t1(const GemvArgs& g, const uint8_t* gsm, uint32_t stage_bytes,
+                                             uint32_t scale_off, uint64_t* full_bar, uint64_t* empty_bar, int s,
+                                             int half, int units) {
+  const int lane = threadIdx.x & 31, NS = g.nstages;
+  uint32_t xh[CPL][16];
+  load_x1<CPL>(g, xh);
+  bool ok = true;
+  int j = s;
+  for (int u = blockIdx.x + s * gridDim.x; u < units; u += NS * gridDim.x, j += NS) {
+    if (!wait_parity(&full_bar[s], (j / NS) & 1)) ok = false;
+    const uint8_t* sc = gsm + (size_t)s * stage_bytes;
+    consume_unit_t1<CPL>(g, sc, sc + scale_off, u % g.ntiles, half, xh, s + 1);
+    __syncwarp();
+    if (lane == 0 && half == 0) mbar_arrive(&empty_bar[s]);
+  }
+  return ok;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(32 * (2 * kMaxStages + 1), 1) nvfp4_gemv_kernel(GemvArgs g) {
   extern __shared__ __align__(128) uint8_t gsm[];
@@ -295,21 +430,11 @@ __global__ void __launch_bounds__(32 * (2 * kMaxStages + 1), 1) nvfp4_gemv_kerne
     // the activations and every output buffer belong to the previous kernels
     griddep_wait();
     const int s = (warp - 1) >> 1, half = (warp - 1) & 1;
-    int j = s;
-    for (int u = blockIdx.x + s * gridDim.x; u < units; u += NS * gridDim.x, j += NS) {
-      if (!wait_parity(&full_bar[s], (j / NS) & 1)) { ok = false; }
-      const uint8_t* sc = gsm + (size_t)s * stage_bytes;
-      const int slice = u / g.ntiles, tile = u % g.ntiles;
-      // both warps of the pair take the same branch (the wait outcome is shared through the
-      // barrier count only when both run): a failed wait skips the work but keeps the barrier
-      const int ngroups = (g.T + 7) / 8;
-      float* xch = xch_all[s][(j / NS) & 1];
-      if (ngroups <= 1) consume_unit<MODE, 1>(g, sc, sc + scale_off, slice, tile, half, xch, s + 1);
-      else if (ngroups == 2) consume_unit<MODE, 2>(g, sc, sc + scale_off, slice, tile, half, xch, s + 1);
-      else consume_unit<MODE, 4>(g, sc, sc + scale_off, slice, tile, half, xch, s + 1);
-      __syncwarp();
-      if (lane == 0 && half == 0) mbar_arrive(&empty_bar[s]);
-    }
+    // one token through the output layer: FMA dot products with x in registers
+    const bool t1 = MODE == kModeHead && g.T == 1 && g.x1 != nullptr && g.nslices == 1;
+    if (t1 && g.KS == 2048) ok = consume_loop_t1<2>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, s, half, units);
+    else if (t1 && g.KS == 1024) ok = consume_loop_t1<1>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, s, half, units);
+    else ok = consume_loop<MODE>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, xch_all, s, half, units);
   }
   if (!ok) latch_status(g.status, MOE_ERR_TIMEOUT);
   __syncthreads();
@@ -667,6 +792,7 @@ moe_status moe_head_forward(moe_dense* x, const void* x_bf16, int T, float* logi
     g.ts0 = x->ts[0];
     g.out = logits + (size_t)t0 * x->rows;
     g.out_ld = x->rows;
+    g.x1 = n == 1 ? xb + (size_t)t0 * x->d : nullptr;
     if (launch_gemv<kModeHead>(g, x->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;

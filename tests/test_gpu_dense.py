@@ -73,6 +73,23 @@ def test_head_small(lib, T):
         lib.moe_dense_destroy(ctx)
 
 
+@pytest.mark.parametrize("d", [1024, 2048])
+def test_head_one_token_fma_path(lib, d):
+    """One token at d_model 1024 or 2048 takes the FMA consumer (x in registers); 33 tokens end
+    with a one-token pass at offset 32, through the same consumer."""
+    vocab = 1008
+    ctx, ow = _head(lib, vocab, d, 64, seed=11)
+    try:
+        for T in (1, 33):
+            xb, x = synth.tokens(synth.MoEShape(d, 1, 1, 128), T, seed=600 + T)
+            out = torch.empty((T, vocab), dtype=torch.float32, device="cuda")
+            lib.moe_head_forward(ctx, xb.cuda(), T, out)
+            assert lib.moe_dense_get_device_status(ctx) == 0
+            _check_logits(out.cpu().numpy(), x.numpy(), ow)
+    finally:
+        lib.moe_dense_destroy(ctx)
+
+
 def test_head_flint(lib):
     vocab, d = synth.FLINT_VOCAB, synth.FLINT.d_model
     ctx, ow = _head(lib, vocab, d, 8, seed=synth.head_seed())
