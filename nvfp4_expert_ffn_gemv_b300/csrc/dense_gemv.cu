@@ -51,11 +51,18 @@ constexpr int kTokPass = 32;          // tokens per pass over the weights (4 col
 // shared-memory bytes for the stage ring: what the 227 KB of a CTA leave after
 // the pair exchange buffers (kMaxStages x 4 KB) and the barriers
 constexpr int kStageBudget = 190464;
-// Stages (= consumer warp pairs) per mode.  The output layer streams the most
-// bytes per call and gains from every stage in flight (8 -> 10 stages: 42.7 ->
-// 39.8 us at one token); the dense FFN passes were measured slower with more.
-constexpr int kHeadStages = 10, kDenseStages = 8;
-__host__ __device__ constexpr int max_stages(int mode) { return mode == 0 ? kHeadStages : kDenseStages; }   // mode 0: the output layer
+// Stages (= consumer warp pairs).  The output layer runs 10 (8 -> 10: 42.7 ->
+// 39.8 us at one token; its 21 warps get 80 registers a thread), and one
+// kernel holds both of its consumers (a one-token kernel of its own compiled
+// worse and ran 0.8 us slower).  The dense gate/up pass at one token (FMA
+// consumers) runs 9 (19 warps keep 96 registers; at 10 it spilled and ran
+// slower); the dense MMA consumers keep 8 (17 warps, 96 registers).
+constexpr int kHeadStages = 10, kGateUpT1Stages = 9, kMmaStages = 8;
+__host__ __device__ constexpr int max_stages(int mode, bool t1) {
+  return mode == 0 ? kHeadStages : (t1 ? kGateUpT1Stages : kMmaStages);   // mode 0: the output layer
+}
+static_assert(kHeadStages <= kMaxStages && kGateUpT1Stages <= kMaxStages && kMmaStages <= kMaxStages,
+              "stage counts above the shared-memory plan");
 static_assert(kMaxStages * 2 * 16 * 32 * 4 + 2 * kMaxStages * 8 + kStageBudget <= 227 * 1024,
               "exchange buffers, barriers and the stage ring must fit one CTA's shared memory");
 
@@ -297,7 +304,7 @@ __device__ __forceinline__ void load_x1(const GemvArgs& g, uint32_t (&xh)[CPL][1
 }
 
 template <int CPL>
-__device__ __forceinline__ void consume_unit_t1(const GemvArgs& g, const uint8_t* sc, const uint8_t* ss, int tile,
+__device__ __forceinline__ void consume_unit_t1_head(const GemvArgs& g, const uint8_t* sc, const uint8_t* ss, int tile,
                                                 int half, const uint32_t (&xh)[CPL][16], int bar_id) {
   const int lane = threadIdx.x & 31;
   const int CB = g.KS / 2, SB = g.KS / 16;
@@ -352,6 +359,76 @@ __device__ __forceinline__ void consume_unit_t1(const GemvArgs& g, const uint8_t
   asm volatile("bar.sync %0, 64;" :: "r"(bar_id) : "memory");
 }
 
+template <int MODE, int CPL>
+__device__ __forceinline__ void consume_unit_t1(const GemvArgs& g, const uint8_t* sc, const uint8_t* ss, int tile,
+                                                int half, const uint32_t (&xh)[CPL][16], float* xch, int bar_id) {
+  const int lane = threadIdx.x & 31;
+  const int CB = g.KS / 2, SB = g.KS / 16;
+  const bool sswz = (SB & 127) == 0;
+  float v[8];
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr) {
+    const int r = half * 8 + rr;
+    const uint8_t* crow = sc + r * CB;
+    const uint8_t* srow = ss + r * SB;
+    float dot = 0.f;
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+      const int j = lane + 32 * q;
+      const uint4 cw = *reinterpret_cast<const uint4*>(crow + swz(j * 16, r & 7));
+      const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
+      float b[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t o[4];
+        cvt_e2m1x8(ws[w], o);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) fma2_mixed(o[p], xh[q][4 * w + p], b[w >> 1][0], b[w >> 1][1]);
+      }
+      const int sb = sswz ? swz(2 * j, r & 7) : 2 * j;
+      const float2 s01 = e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t*>(srow + sb));
+      dot = fmaf(b[0][0] + b[0][1], s01.x, dot);
+      dot = fmaf(b[1][0] + b[1][1], s01.y, dot);
+    }
+    v[rr] = dot;
+  }
+  // transposing sum over the warp: after the xor-16, -8 and -4 steps lane l
+  // holds a partial of row (l >> 2) & 7, completed by the xor-2 and -1 steps
+  const int b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+  float w4[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b4 ? v[i + 4] : v[i], send = b4 ? v[i] : v[i + 4];
+    w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+  float w2[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b3 ? w4[i + 2] : w4[i], send = b3 ? w4[i] : w4[i + 2];
+    w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float t = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+  t += __shfl_xor_sync(0xffffffffu, t, 2);
+  t += __shfl_xor_sync(0xffffffffu, t, 1);
+  // dense gate/up: warp 0 of the pair has the gate rows, warp 1 the up rows of
+  // hidden units tile * 8 + r; they meet in shared memory for SwiGLU
+  if (half && (lane & 3) == 0) xch[lane >> 2] = t;
+  asm volatile("bar.sync %0, 64;" :: "r"(bar_id) : "memory");
+  if (half) return;
+  const float un = g.unshift[0];
+  float a = 0.f;
+  if ((lane & 3) == 0) {
+    const float hv = silu_f(t * g.ts0 * un) * (xch[lane >> 2] * g.ts1 * un);
+    g.out[tile * 8 + (lane >> 2)] = hv;
+    a = fabsf(hv) == fabsf(hv) ? fabsf(hv) : 0.f;   // NaN left out of max |h|, as fmaxf does
+  }
+  uint32_t m = __float_as_uint(a);
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+  if (lane == 0 && m != 0u) atomicMax(g.hmax, m);
+}
+
 // The consumer loops of stage s (warps 2s + 1 and 2s + 2, one per half).  Both
 // warps of the pair take the same path (the wait outcome is shared through the
 // barrier count only when both run): a failed wait skips nothing but is reported.
@@ -378,9 +455,9 @@ __device__ __forceinline__ bool consume_loop(const GemvArgs& g, const uint8_t* g
 }
 
 template <int CPL>
-__device__ __noinline__ bool consume_loop_t1(const GemvArgs& g, const uint8_t* gsm, uint32_t stage_bytes,
-                                             uint32_t scale_off, uint64_t* full_bar, uint64_t* empty_bar, int s,
-                                             int half, int units) {
+__device__ __noinline__ bool consume_loop_t1_head(const GemvArgs& g, const uint8_t* gsm, uint32_t stage_bytes,
+                                                  uint32_t scale_off, uint64_t* full_bar, uint64_t* empty_bar, int s,
+                                                  int half, int units) {
   const int lane = threadIdx.x & 31, NS = g.nstages;
   uint32_t xh[CPL][16];
   load_x1<CPL>(g, xh);
@@ -389,19 +466,42 @@ __device__ __noinline__ bool consume_loop_t1(const GemvArgs& g, const uint8_t* g
   for (int u = blockIdx.x + s * gridDim.x; u < units; u += NS * gridDim.x, j += NS) {
     if (!wait_parity(&full_bar[s], (j / NS) & 1)) ok = false;
     const uint8_t* sc = gsm + (size_t)s * stage_bytes;
-    consume_unit_t1<CPL>(g, sc, sc + scale_off, u % g.ntiles, half, xh, s + 1);
+    consume_unit_t1_head<CPL>(g, sc, sc + scale_off, u % g.ntiles, half, xh, s + 1);
     __syncwarp();
     if (lane == 0 && half == 0) mbar_arrive(&empty_bar[s]);
   }
   return ok;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(32 * (2 * max_stages(MODE) + 1), 1) nvfp4_gemv_kernel(GemvArgs g) {
+template <int MODE, int CPL>
+__device__ __noinline__ bool consume_loop_t1(const GemvArgs& g, const uint8_t* gsm, uint32_t stage_bytes,
+                                             uint32_t scale_off, uint64_t* full_bar, uint64_t* empty_bar,
+                                             float (*xch_all)[2][16 * 32], int s, int half, int units) {
+  const int lane = threadIdx.x & 31, NS = g.nstages;
+  uint32_t xh[CPL][16];
+  load_x1<CPL>(g, xh);
+  bool ok = true;
+  int j = s;
+  for (int u = blockIdx.x + s * gridDim.x; u < units; u += NS * gridDim.x, j += NS) {
+    if (!wait_parity(&full_bar[s], (j / NS) & 1)) ok = false;
+    const uint8_t* sc = gsm + (size_t)s * stage_bytes;
+    float* xch = nullptr;
+    if constexpr (MODE == kModeGateUp) xch = xch_all[s][(j / NS) & 1];
+    consume_unit_t1<MODE, CPL>(g, sc, sc + scale_off, u % g.ntiles, half, xh, xch, s + 1);
+    __syncwarp();
+    if (lane == 0 && half == 0) mbar_arrive(&empty_bar[s]);
+  }
+  return ok;
+}
+
+// T1: one token through the dense gate/up pass on the FMA consumers (d_model
+// 1024 or 2048).  The output layer picks its consumer at run time instead.
+template <int MODE, bool T1>
+__global__ void __launch_bounds__(32 * (2 * max_stages(MODE, T1) + 1), 1) nvfp4_gemv_kernel(GemvArgs g) {
   extern __shared__ __align__(128) uint8_t gsm[];
-  __shared__ __align__(8) uint64_t full_bar[max_stages(MODE)], empty_bar[max_stages(MODE)];
+  __shared__ __align__(8) uint64_t full_bar[max_stages(MODE, T1)], empty_bar[max_stages(MODE, T1)];
   // partial sums a warp pair exchanges: [stage][unit parity][16 values][32 lanes]
-  __shared__ float xch_all[max_stages(MODE)][2][16 * 32];
+  __shared__ float xch_all[max_stages(MODE, T1)][2][16 * 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = g.nstages;
   const uint32_t rcodes = (uint32_t)g.KS / 2, rscales = (uint32_t)g.KS / 16;     // bytes per row
@@ -439,11 +539,22 @@ __global__ void __launch_bounds__(32 * (2 * max_stages(MODE) + 1), 1) nvfp4_gemv
     // the activations and every output buffer belong to the previous kernels
     griddep_wait();
     const int s = (warp - 1) >> 1, half = (warp - 1) & 1;
-    // one token through the output layer: FMA dot products with x in registers
-    const bool t1 = MODE == kModeHead && g.T == 1 && g.x1 != nullptr && g.nslices == 1;
-    if (t1 && g.KS == 2048) ok = consume_loop_t1<2>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, s, half, units);
-    else if (t1 && g.KS == 1024) ok = consume_loop_t1<1>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, s, half, units);
-    else ok = consume_loop<MODE>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, xch_all, s, half, units);
+    const bool head_t1 = MODE == kModeHead && g.T == 1 && g.x1 != nullptr && g.nslices == 1;
+    if constexpr (MODE == kModeHead) {
+      if (head_t1 && g.KS == 2048)
+        ok = consume_loop_t1_head<2>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, s, half, units);
+      else if (head_t1 && g.KS == 1024)
+        ok = consume_loop_t1_head<1>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, s, half, units);
+      else
+        ok = consume_loop<MODE>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, xch_all, s, half, units);
+    } else if constexpr (T1 && MODE == kModeGateUp) {
+      if (g.KS == 2048)
+        ok = consume_loop_t1<MODE, 2>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, xch_all, s, half, units);
+      else
+        ok = consume_loop_t1<MODE, 1>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, xch_all, s, half, units);
+    } else {
+      ok = consume_loop<MODE>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, xch_all, s, half, units);
+    }
   }
   if (!ok) latch_status(g.status, MOE_ERR_TIMEOUT);
   __syncthreads();
@@ -601,20 +712,28 @@ __global__ void slice_rows_kernel(const uint8_t* __restrict__ src, int d, size_t
     dst[((size_t)s * d + r) * sb + i] = src[(size_t)r * row_bytes + (size_t)s * sb + i];
 }
 
-int stages_for(int KS, int mode) {
-  const int cap = mode == kModeHead ? kHeadStages : kDenseStages;
+int stages_for(int KS, int mode, bool t1) {
+  const int cap = max_stages(mode, t1);
   const int n = kStageBudget / (int)stage_bytes_of(KS);
   return n > cap ? cap : n;
 }
 
-size_t gemv_smem(int KS, int mode) { return (size_t)stages_for(KS, mode) * stage_bytes_of(KS); }
+size_t gemv_smem(int KS, int mode, bool t1) { return (size_t)stages_for(KS, mode, t1) * stage_bytes_of(KS); }
 
 template <int MODE>
 cudaError_t launch_gemv(GemvArgs g, int sm_count, cudaStream_t s) {
   const int units = g.ntiles * g.nslices;
   const int grid = units < sm_count ? units : sm_count;
-  g.nstages = stages_for(g.KS, MODE);
-  return launch_pdl(nvfp4_gemv_kernel<MODE>, dim3(grid), dim3(32 * (2 * g.nstages + 1)), gemv_smem(g.KS, MODE), s, g);
+  if constexpr (MODE == kModeGateUp) {
+    if (g.T == 1 && g.x1 != nullptr && g.nslices == 1 && (g.KS == 1024 || g.KS == 2048)) {
+      g.nstages = stages_for(g.KS, MODE, true);
+      return launch_pdl(nvfp4_gemv_kernel<MODE, true>, dim3(grid), dim3(32 * (2 * g.nstages + 1)),
+                        gemv_smem(g.KS, MODE, true), s, g);
+    }
+  }
+  g.nstages = stages_for(g.KS, MODE, false);
+  return launch_pdl(nvfp4_gemv_kernel<MODE, false>, dim3(grid), dim3(32 * (2 * g.nstages + 1)),
+                    gemv_smem(g.KS, MODE, false), s, g);
 }
 
 }  // namespace
@@ -704,9 +823,11 @@ moe_status alloc_dense(moe_dense* x) {
 cudaError_t set_gemv_smem() {
   cudaError_t e = cudaSuccess;
   const int lim = kStageBudget;   // every ring fits: stages_for() fills at most this many bytes
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeHead>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeHead, false>, a, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeGateUp, false>, a, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeGateUp, true>, a, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeDown, false>, a, lim);
   return e;
 }
 
@@ -911,6 +1032,7 @@ moe_status moe_ffn_forward(moe_dense* x, const void* x_bf16, int T, void* y_bf16
     g.out = x->h;
     g.out_ld = f;
     g.hmax = x->hmax;
+    g.x1 = n == 1 ? xb + (size_t)t0 * d : nullptr;
     if (launch_gemv<kModeGateUp>(g, x->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_pdl(prep_h_kernel, dim3((unsigned)((f + kPrepHChunk - 1) / kPrepHChunk), (unsigned)rows_read(n)),
                    dim3(256), 0, s, (const float*)x->h, n, f, (const uint32_t*)x->hmax, x->h_hi, x->h_lo,
