@@ -54,14 +54,14 @@ constexpr int kStageBudget = 190464;
 // Stages (= consumer warp pairs).  The output layer runs 10 (8 -> 10: 42.7 ->
 // 39.8 us at one token; its 21 warps get 80 registers a thread), and one
 // kernel holds both of its consumers (a one-token kernel of its own compiled
-// worse and ran 0.8 us slower).  The dense gate/up pass at one token (FMA
-// consumers) runs 9 (19 warps keep 96 registers; at 10 it spilled and ran
+// worse and ran 0.8 us slower).  The dense passes at one token (FMA
+// consumers) run 9 (19 warps keep 96 registers; at 10 gate/up spilled and ran
 // slower); the dense MMA consumers keep 8 (17 warps, 96 registers).
-constexpr int kHeadStages = 10, kGateUpT1Stages = 9, kMmaStages = 8;
+constexpr int kHeadStages = 10, kDenseT1Stages = 9, kMmaStages = 8;
 __host__ __device__ constexpr int max_stages(int mode, bool t1) {
-  return mode == 0 ? kHeadStages : (t1 ? kGateUpT1Stages : kMmaStages);   // mode 0: the output layer
+  return mode == 0 ? kHeadStages : (t1 ? kDenseT1Stages : kMmaStages);   // mode 0: the output layer
 }
-static_assert(kHeadStages <= kMaxStages && kGateUpT1Stages <= kMaxStages && kMmaStages <= kMaxStages,
+static_assert(kHeadStages <= kMaxStages && kDenseT1Stages <= kMaxStages && kMmaStages <= kMaxStages,
               "stage counts above the shared-memory plan");
 static_assert(kMaxStages * 2 * 16 * 32 * 4 + 2 * kMaxStages * 8 + kStageBudget <= 227 * 1024,
               "exchange buffers, barriers and the stage ring must fit one CTA's shared memory");
@@ -85,7 +85,8 @@ struct GemvArgs {
   int nstages;             // stages = consumer warps
   int* status;
   int dbg;
-  const __nv_bfloat16* x1; // head at one token: the token's bf16 row (x in registers, FMA dot products)
+  const __nv_bfloat16* x1; // head / gate/up at one token: the token's bf16 row (x in registers, FMA dot products)
+  const float* h1;         // down at one token: the token's fp32 h row (FMA dot products, no hi/lo split)
 };
 
 __device__ __forceinline__ uint2 ldg64(const uint8_t* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
@@ -494,8 +495,102 @@ __device__ __noinline__ bool consume_loop_t1(const GemvArgs& g, const uint8_t* g
   return ok;
 }
 
-// T1: one token through the dense gate/up pass on the FMA consumers (d_model
-// 1024 or 2048).  The output layer picks its consumer at run time instead.
+// One token through the dense down projection (K slices of 2048): each warp
+// of the pair takes one half of the unit's slice for all 16 rows, with that
+// half of h (fp32, 32 values a lane) in registers, requested before the
+// stage wait.  A code is expanded to exact f16 by the hardware cvt and then
+// to fp32, so each product is one fp32 FMA with h (the MMA path splits h into
+// f16 hi + lo instead); the block scale multiplies each 16-term partial.  The
+// rows are summed over the warp in two groups of 8 (9 shuffles each), the pair
+// adds its halves through shared memory (first + second), and warp 0 writes
+// the slice's partial outputs.
+__device__ __forceinline__ void consume_unit_t1_down(const GemvArgs& g, const uint8_t* sc, const uint8_t* ss,
+                                                     int slice, int tile, int half, const float (&hv)[32],
+                                                     float* xch, int bar_id) {
+  const int lane = threadIdx.x & 31;
+  constexpr int CB = 1024, SB = 128;   // code / scale bytes of a 2048-wide row
+  const int b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+  float t2[2];
+#pragma unroll
+  for (int grp = 0; grp < 2; ++grp) {
+    float v[8];
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) {
+      const int r = grp * 8 + rr;
+      const uint4 cw = *reinterpret_cast<const uint4*>(sc + r * CB + swz(half * 512 + lane * 16, r & 7));
+      const float2 s01 =
+          e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t*>(ss + r * SB + swz(half * 64 + lane * 2, r & 7)));
+      const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
+      float b[2] = {0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t o[4];
+        cvt_e2m1x8(ws[w], o);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const float2 f = f16x2_to_f32x2(o[p]);
+          b[w >> 1] = fmaf(f.x, hv[8 * w + 2 * p], b[w >> 1]);
+          b[w >> 1] = fmaf(f.y, hv[8 * w + 2 * p + 1], b[w >> 1]);
+        }
+      }
+      v[rr] = fmaf(b[0], s01.x, b[1] * s01.y);
+    }
+    // transposing sum over the warp (as the output layer's): lane 4r ends with row grp * 8 + r
+    float w4[4], w2[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w4[i] = (b4 ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[i + 4], 16);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      w2[i] = (b3 ? w4[i + 2] : w4[i]) + __shfl_xor_sync(0xffffffffu, b3 ? w4[i] : w4[i + 2], 8);
+    float t = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+    t += __shfl_xor_sync(0xffffffffu, t, 2);
+    t += __shfl_xor_sync(0xffffffffu, t, 1);
+    t2[grp] = t;
+    asm volatile("" ::: "memory");   // the second group's loads after the first group's sums
+  }
+  if (half && (lane & 3) == 0) {
+    xch[lane >> 2] = t2[0];
+    xch[8 + (lane >> 2)] = t2[1];
+  }
+  asm volatile("bar.sync %0, 64;" :: "r"(bar_id) : "memory");
+  if (!half && (lane & 3) == 0) {
+    float* dst = g.out + (size_t)slice * g.out_ld + tile * 16 + (lane >> 2);
+    dst[0] = (t2[0] + xch[lane >> 2]) * g.ts0;
+    dst[8] = (t2[1] + xch[8 + (lane >> 2)]) * g.ts0;
+  }
+}
+
+__device__ __noinline__ bool consume_loop_t1_down(const GemvArgs& g, const uint8_t* gsm, uint32_t stage_bytes,
+                                                  uint32_t scale_off, uint64_t* full_bar, uint64_t* empty_bar,
+                                                  float (*xch_all)[2][16 * 32], int s, int half, int units) {
+  const int lane = threadIdx.x & 31, NS = g.nstages;
+  bool ok = true;
+  int j = s;
+  for (int u = blockIdx.x + s * gridDim.x; u < units; u += NS * gridDim.x, j += NS) {
+    const int slice = u / g.ntiles, tile = u % g.ntiles;
+    float hv[32];
+    const float4* hp = reinterpret_cast<const float4*>(g.h1 + (size_t)slice * 2048 + half * 1024 + lane * 32);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 q = hp[i];
+      hv[4 * i] = q.x;
+      hv[4 * i + 1] = q.y;
+      hv[4 * i + 2] = q.z;
+      hv[4 * i + 3] = q.w;
+    }
+    if (!wait_parity(&full_bar[s], (j / NS) & 1)) ok = false;
+    const uint8_t* sc = gsm + (size_t)s * stage_bytes;
+    consume_unit_t1_down(g, sc, sc + scale_off, slice, tile, half, hv, xch_all[s][(j / NS) & 1], s + 1);
+    __syncwarp();
+    if (lane == 0 && half == 0) mbar_arrive(&empty_bar[s]);
+  }
+  return ok;
+}
+
+// T1: one token through the dense gate/up pass (d_model 1024 or 2048) or the
+// dense down pass (K slices of 2048) on the FMA consumers.  The output layer
+// picks its consumer at run time instead.
 template <int MODE, bool T1>
 __global__ void __launch_bounds__(32 * (2 * max_stages(MODE, T1) + 1), 1) nvfp4_gemv_kernel(GemvArgs g) {
   extern __shared__ __align__(128) uint8_t gsm[];
@@ -547,6 +642,8 @@ __global__ void __launch_bounds__(32 * (2 * max_stages(MODE, T1) + 1), 1) nvfp4_
         ok = consume_loop_t1_head<1>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, s, half, units);
       else
         ok = consume_loop<MODE>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, xch_all, s, half, units);
+    } else if constexpr (T1 && MODE == kModeDown) {
+      ok = consume_loop_t1_down(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, xch_all, s, half, units);
     } else if constexpr (T1 && MODE == kModeGateUp) {
       if (g.KS == 2048)
         ok = consume_loop_t1<MODE, 2>(g, gsm, stage_bytes, scale_off, full_bar, empty_bar, xch_all, s, half, units);
@@ -724,6 +821,13 @@ template <int MODE>
 cudaError_t launch_gemv(GemvArgs g, int sm_count, cudaStream_t s) {
   const int units = g.ntiles * g.nslices;
   const int grid = units < sm_count ? units : sm_count;
+  if constexpr (MODE == kModeDown) {
+    if (g.T == 1 && g.h1 != nullptr && g.KS == 2048) {
+      g.nstages = stages_for(g.KS, MODE, true);
+      return launch_pdl(nvfp4_gemv_kernel<MODE, true>, dim3(grid), dim3(32 * (2 * g.nstages + 1)),
+                        gemv_smem(g.KS, MODE, true), s, g);
+    }
+  }
   if constexpr (MODE == kModeGateUp) {
     if (g.T == 1 && g.x1 != nullptr && g.nslices == 1 && (g.KS == 1024 || g.KS == 2048)) {
       g.nstages = stages_for(g.KS, MODE, true);
@@ -803,7 +907,11 @@ bool matrix_ok(const moe_matrix* m) { return m && m->codes && m->scales && m->te
 // K slices of the dense down projection: the largest K slice <= 2304 that is a
 // multiple of 256 (a code row of the slice is whole 128-byte swizzle segments)
 // and divides f (so a stage of 16 rows x K slice stays ~20 KB).
+// K slices of the dense down projection: 2048 wide when they divide d_ff
+// (the width the one-token FMA consumer takes), else the widest multiple of
+// 256 up to 2304 that does.
 int down_slices(int f) {
+  if (f % 2048 == 0) return f / 2048;
   for (int ks = 2304; ks >= 256; ks -= 256)
     if (f % ks == 0) return f / ks;
   return -1;
@@ -828,6 +936,7 @@ cudaError_t set_gemv_smem() {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeGateUp, false>, a, lim);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeGateUp, true>, a, lim);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeDown, false>, a, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(nvfp4_gemv_kernel<kModeDown, true>, a, lim);
   return e;
 }
 
@@ -1034,11 +1143,15 @@ moe_status moe_ffn_forward(moe_dense* x, const void* x_bf16, int T, void* y_bf16
     g.hmax = x->hmax;
     g.x1 = n == 1 ? xb + (size_t)t0 * d : nullptr;
     if (launch_gemv<kModeGateUp>(g, x->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_pdl(prep_h_kernel, dim3((unsigned)((f + kPrepHChunk - 1) / kPrepHChunk), (unsigned)rows_read(n)),
+    // one token with 2048-wide K slices: the down pass reads h (fp32) itself, no hi / lo split
+    const bool h_direct = n == 1 && x->KS == 2048;
+    if (!h_direct &&
+        launch_pdl(prep_h_kernel, dim3((unsigned)((f + kPrepHChunk - 1) / kPrepHChunk), (unsigned)rows_read(n)),
                    dim3(256), 0, s, (const float*)x->h, n, f, (const uint32_t*)x->hmax, x->h_hi, x->h_lo,
                    x->hun) != cudaSuccess)
       return MOE_ERR_CUDA;
     GemvArgs dn = base_args(x, n);
+    dn.h1 = h_direct ? x->h : nullptr;
     dn.codes = x->dn_codes;
     dn.scales = x->dn_scales;
     dn.slice_codes = (size_t)d * x->KS / 2;

@@ -124,12 +124,27 @@ def _check_ffn(lib, ctx, oracle, shape, T, seed, residual):
 
 @pytest.mark.parametrize("T", [1, 7, 40])
 def test_dense_ffn_small(lib, T):
-    d, f = 256, 4608          # two K slices of 2304 in the down projection
+    d, f = 256, 4608          # two K slices of 2304 in the down projection (MMA consumers at every T)
     shape = synth.MoEShape(d, 1, 1, 128)
     ctx, oracle = _ffn(lib, d, f, 64, seed=9)
     try:
         _check_ffn(lib, ctx, oracle, shape, T, seed=700 + T, residual=0)
         _check_ffn(lib, ctx, oracle, shape, T, seed=800 + T, residual=1)
+    finally:
+        lib.moe_dense_destroy(ctx)
+
+
+@pytest.mark.parametrize("T", [1, 33])
+def test_dense_ffn_one_token_fma_paths(lib, T):
+    """d_model 1024 and 2048-wide K slices: one token takes the FMA consumers of both passes (h read
+    as fp32 by the down pass, no hi / lo split); 33 tokens run a 32-token MMA pass, then a one-token
+    pass at offset 32 through the FMA consumers."""
+    d, f = 1024, 4096         # two K slices of 2048 in the down projection
+    shape = synth.MoEShape(d, 1, 1, 128)
+    ctx, oracle = _ffn(lib, d, f, 64, seed=13)
+    try:
+        _check_ffn(lib, ctx, oracle, shape, T, seed=900 + T, residual=0)
+        _check_ffn(lib, ctx, oracle, shape, T, seed=950 + T, residual=1)
     finally:
         lib.moe_dense_destroy(ctx)
 
