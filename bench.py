@@ -621,6 +621,7 @@ def run_dense(args):
         ge.replay()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(timed(ge, replays))
+    per_fwd = lib.moe_dense_kernels_per_forward(ctxs[0], T)
     for c in ctxs:
         lib.moe_dense_destroy(c)
     if rank != 0:
@@ -639,7 +640,7 @@ def run_dense(args):
                    "tokens_per_step": T, "copies": n_copies,
                    "l2": f"{n_copies} rotating weight copies ({n_copies * alg / 1e6:.0f} MB, above the 126 MB L2)",
                    "parallelism": "independent replicas" if world > 1 else "single GPU"},
-        "gpu_launches": K * (2 if head else 5),
+        "gpu_launches": K * per_fwd,
         "clocks": clk.summary(),
         "roofline": {"kernel": "streaming NVFP4 GEMV (lm_head)" if head else
                      "dense FFN: gate/up GEMV + SwiGLU, down GEMV, slice reduction",

@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTS = ("moe_init", "moe_route", "moe_route_noalloc", "moe_forward_decode", "moe_forward_prefill", "moe_quantize_nvfp4",
            "moe_debug_prefill_h", "moe_debug_routing", "moe_set_profile_events", "moe_set_debug", "moe_debug_logits",
            "moe_debug_wait_selftest", "moe_debug_fail_alloc", "moe_head_init", "moe_head_forward", "moe_ffn_init",
-           "moe_ffn_forward", "moe_dense_get_device_status", "moe_dense_destroy", "moe_get_device_status",
+           "moe_ffn_forward", "moe_dense_get_device_status", "moe_dense_kernels_per_forward", "moe_dense_destroy",
+           "moe_get_device_status",
            "moe_kernels_per_forward", "moe_destroy", "moe_status_string")
 MOE_DEBUG_KEEP_LOGITS = 1
 MOE_DEBUG_FORCE_TIMEOUT = 2
@@ -83,6 +84,7 @@ def _load():
         "moe_ffn_init": (i, [i, i, p(moe_matrix), p(moe_matrix), p(moe_matrix), i, i, p(vp)]),
         "moe_ffn_forward": (i, [vp, vp, i, vp, i, vp]),
         "moe_dense_get_device_status": (i, [vp]),
+        "moe_dense_kernels_per_forward": (i, [vp, i]),
         "moe_dense_destroy": (i, [vp]),
         "moe_get_device_status": (i, [vp]),
         "moe_kernels_per_forward": (i, [vp, i, i]),
@@ -234,6 +236,10 @@ def moe_ffn_forward(ctx, x, T: int, y, residual: int = 0, stream=None) -> None:
 
 def moe_dense_get_device_status(ctx) -> int:
     return int(_lib.moe_dense_get_device_status(ctx))
+
+
+def moe_dense_kernels_per_forward(ctx, T: int) -> int:
+    return int(_lib.moe_dense_kernels_per_forward(ctx, int(T)))
 
 
 def moe_dense_destroy(ctx) -> None:

@@ -1184,6 +1184,16 @@ moe_status moe_dense_get_device_status(moe_dense* x) {
   return static_cast<moe_status>(v);
 }
 
+int moe_dense_kernels_per_forward(moe_dense* x, int T) {
+  if (!x || T <= 0) return 0;
+  int n = 0;
+  for (int t0 = 0; t0 < T; t0 += kTokPass) {
+    const int m = T - t0 < kTokPass ? T - t0 : kTokPass;
+    n += x->kind == 0 ? 2 : (m == 1 && x->KS == 2048 ? 4 : 5);
+  }
+  return n;
+}
+
 moe_status moe_dense_destroy(moe_dense* x) {
   if (!x) return MOE_OK;
   cudaSetDevice(x->device);

@@ -74,3 +74,4 @@ def test_calls_reject_null_context_and_bad_sizes():
     assert lib.moe_quantize_nvfp4(0x1004, 1, 4, 32, 0x2000, 0x3000, 0x4000, None) == 1
     assert lib.moe_quantize_nvfp4(0x1000, 0, 4, 32, 0x2000, 0x3000, 0x4000, None) == 1
     assert lib.moe_kernels_per_forward(None, 1, 0) == 0
+    assert lib.moe_dense_kernels_per_forward(None, 1) == 0

@@ -159,6 +159,21 @@ def test_dense_ffn_flint(lib):
         lib.moe_dense_destroy(ctx)
 
 
+def test_dense_kernel_counts(lib):
+    """The launches a forward makes, as the library reports them for accounting: 2 per 32-token
+    pass of the output layer; 5 per dense FFN pass, 4 for a one-token pass with 2048-wide K slices."""
+    head, _ = _head(lib, 400, 256, 64, seed=7)
+    ffn_2048, _ = _ffn(lib, 1024, 4096, 64, seed=13)
+    ffn_2304, _ = _ffn(lib, 256, 4608, 64, seed=9)
+    try:
+        assert [lib.moe_dense_kernels_per_forward(head, T) for T in (0, 1, 32, 33)] == [0, 2, 2, 4]
+        assert [lib.moe_dense_kernels_per_forward(ffn_2048, T) for T in (1, 2, 33)] == [4, 5, 9]
+        assert [lib.moe_dense_kernels_per_forward(ffn_2304, T) for T in (1, 33)] == [5, 10]
+    finally:
+        for c in (head, ffn_2048, ffn_2304):
+            lib.moe_dense_destroy(c)
+
+
 def test_dense_rejects_bad_arguments(lib):
     z = torch.zeros(16, dtype=torch.uint8, device="cuda")
     m = dict(codes=z, scales=z, tensor_scale=torch.zeros(1, device="cuda"))
