@@ -396,8 +396,9 @@ def run_ours(args):
     e2e_ms = timed(ge, replays)
     e2e_ms = max_over_ranks(e2e_ms)
     if not prefill:
-        # the decode kernels are deterministic: the host results equal the device-resident run's
-        if not torch.equal(yh, y[:chunk].cpu()):
+        # the decode kernels are deterministic: the host results equal the device-resident run's,
+        # bit for bit (compared as bit patterns, so NaN outputs match too)
+        if not torch.equal(yh.view(torch.int16), y[:chunk].cpu().view(torch.int16)):
             raise RuntimeError("end-to-end results differ from the device-resident run")
 
     # algorithmic bytes of a batched-decode step: every distinct chosen expert once, plus the shared one
@@ -440,6 +441,9 @@ def run_ours(args):
         "config": {"workload": args.workload if n_layers == wl["layers"] else f"{args.workload} ({n_layers} layers)",
                    "d_model": D_MODEL, "n_experts": N_EXP, "top_k": TOP_K,
                    "n_shared": N_SHARED, "d_ff": D_FF, "tokens_per_step": T, "layers": n_layers,
+                   **({"activations": "residual stream without normalisation: it overflows fp32 at layer 25, "
+                                      "later layers see NaN and route to experts 0-5 (7 experts streamed per "
+                                      "layer either way)"} if stack else {}),
                    "l2": ("47 distinct layers, ~21 GB of weights" if stack else
                           f"{n_layers} rotating layer copies ({n_layers * 0.455:.1f} GB of NVFP4 experts, far above "
                           "the 126 MB L2): no weight is re-read from L2 between steps"),
