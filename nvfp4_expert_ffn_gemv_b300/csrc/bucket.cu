@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kGroupChunks * 32) bucket_count_kernel(Routing
     int ej[8];
     if (valid) {
       for (int j = 0; j < k; ++j) {
-        int e = __ldg(r.idx + (size_t)t * k + j);
+        int e = __ldcg(r.idx + (size_t)t * k + j);
         if (e < 0 || e >= E) { latch_status(status, MOE_ERR_DEVICE_CHECK); e = 0; }
         ej[j] = e;
         atomicOr(&mask[warp][e], 1u << lane);
@@ -328,13 +328,13 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(Routing r, int T, i
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s < T * k) {
     const int t = s / k;
-    int e = __ldg(r.idx + s);
+    int e = __ldcg(r.idx + s);
     if (e < 0 || e >= E) e = 0;   // reported by the count kernel
-    const int p = __ldg(r.offsets + e) + __ldg(r.group_cnt + (size_t)(t >> 8) * E + e) +
-                  __ldg(r.chunk_cnt + (size_t)(t >> 5) * E + e) + __ldg(r.rank + s);
+    const int p = __ldcg(r.offsets + e) + __ldcg(r.group_cnt + (size_t)(t >> 8) * E + e) +
+                  __ldcg(r.chunk_cnt + (size_t)(t >> 5) * E + e) + __ldcg(r.rank + s);
     r.slot_pos[s] = p;
     r.pos_tok[p] = t;
-    r.pos_w[p] = __ldg(r.w + s);
+    r.pos_w[p] = __ldcg(r.w + s);
   } else if (s < T * k + S * T) {
     const int q = s - T * k;
     r.pos_tok[T * k + q] = q % T;

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(256) xprep_kernel(MmaArgs g) {
   const uint4* src = reinterpret_cast<const uint4*>(g.x + (size_t)t * d);
   float m = 0.f;
   for (int i = lane; i < d / 8; i += 32) {
-    const uint4 v = __ldg(src + i);
+    const uint4 v = __ldcg(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(256) xprep_kernel(MmaArgs g) {
   const float sc = pow2i(shift);
   uint8_t* dst = g.x16 + (size_t)t * d * 2;
   for (int i = lane; i < d / 8; i += 32) {
-    const uint4 v = __ldg(src + i);
+    const uint4 v = __ldcg(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t hv[4];
 #pragma unroll

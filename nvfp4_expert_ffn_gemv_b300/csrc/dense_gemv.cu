@@ -89,7 +89,9 @@ struct GemvArgs {
   const float* h1;         // down at one token: the token's fp32 h row (FMA dot products, no hi/lo split)
 };
 
-__device__ __forceinline__ uint2 ldg64(const uint8_t* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+// B operand (written by the kernel before, which may still run while this one
+// starts): coherent loads through L2, never the non-coherent read-only path
+__device__ __forceinline__ uint2 ldg64(const uint8_t* p) { return __ldcg(reinterpret_cast<const uint2*>(p)); }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -293,7 +295,7 @@ __device__ __forceinline__ void load_x1(const GemvArgs& g, uint32_t (&xh)[CPL][1
     const uint4* src = reinterpret_cast<const uint4*>(g.x1 + (size_t)(lane + 32 * q) * 32);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 v = __ldg(src + i);
+      const uint4 v = __ldcg(src + i);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
@@ -676,9 +678,8 @@ __device__ __forceinline__ float block_max256(float m, uint32_t* red) {
 
 // bf16 x [T][K] -> prescaled f16 in the permuted chunk order, one CTA per row
 // of the B operand (rows T .. rows_read(T) - 1 zero); unshift[t] = 2^-shift.
-__global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* __restrict__ x, int T, int K,
-                                                     uint8_t* __restrict__ out, float* __restrict__ unshift,
-                                                     uint32_t* __restrict__ hmax) {
+__global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* x, int T, int K, uint8_t* out,
+                                                     float* unshift, uint32_t* hmax) {
   __shared__ uint32_t red[8];
   griddep_launch();
   griddep_wait();
@@ -693,7 +694,7 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* __rest
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * K);
   float m = 0.f;
   for (int i = threadIdx.x; i < K / 8; i += 256) {
-    const uint4 v = __ldg(src + i);
+    const uint4 v = __ldcg(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -702,7 +703,7 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* __rest
   const int shift = prescale_shift(__float_as_uint(block_max256(m, red)));
   const float sc = pow2i(shift);
   for (int i = threadIdx.x; i < K / 8; i += 256) {
-    const uint4 v = __ldg(src + i);
+    const uint4 v = __ldcg(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t hv[4];
 #pragma unroll
@@ -723,9 +724,8 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* __rest
 // hmax[t], so a row is split over K / 2048 CTAs (blockIdx.x = chunk,
 // blockIdx.y = row; rows T.. are zero).
 constexpr int kPrepHChunk = 2048;
-__global__ void __launch_bounds__(256) prep_h_kernel(const float* __restrict__ h, int T, int K,
-                                                     const uint32_t* __restrict__ hmax, uint8_t* __restrict__ hi,
-                                                     uint8_t* __restrict__ lo, float* __restrict__ unshift) {
+__global__ void __launch_bounds__(256) prep_h_kernel(const float* h, int T, int K, const uint32_t* hmax,
+                                                     uint8_t* hi, uint8_t* lo, float* unshift) {
   griddep_launch();
   griddep_wait();
   const int t = blockIdx.y;
@@ -758,9 +758,8 @@ __global__ void __launch_bounds__(256) prep_h_kernel(const float* __restrict__ h
 }
 
 // y[t][r] = bf16(sum over the S K slices, in order, of partial[s][t][r] (+ x[t][r]))
-__global__ void __launch_bounds__(256) reduce_down_kernel(const float* __restrict__ part, int S, int T, int d,
-                                                          const __nv_bfloat16* __restrict__ x, int residual,
-                                                          __nv_bfloat16* __restrict__ y) {
+__global__ void __launch_bounds__(256) reduce_down_kernel(const float* part, int S, int T, int d,
+                                                          const __nv_bfloat16* x, int residual, __nv_bfloat16* y) {
   griddep_launch();
   griddep_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;

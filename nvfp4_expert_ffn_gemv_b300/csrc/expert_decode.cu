@@ -350,9 +350,9 @@ cudaError_t prepare_decode_kernels(const moe_ctx* c) {
 // Fixed summation order (j ascending, then shared), so results are deterministic.
 // ---------------------------------------------------------------------------
 namespace {
-__global__ void __launch_bounds__(256) combine_kernel(Routing r, const float* __restrict__ yexp,
-                                                      const __nv_bfloat16* __restrict__ x,
-                                                      __nv_bfloat16* __restrict__ y, int T, int d,
+__global__ void __launch_bounds__(256) combine_kernel(Routing r, const float* yexp,
+                                                      const __nv_bfloat16* x,
+                                                      __nv_bfloat16* y, int T, int d,
                                                       int k, int S, int residual) {
   pdl_trigger();
   pdl_wait();

@@ -4,7 +4,11 @@
 // in the stream is still running.  It must call pdl_wait() before it reads or
 // writes anything an earlier kernel of the stream touches; what it does before
 // that may only read data written before the forward began (the weights), or
-// its own shared memory.  pdl_trigger() lets the next kernel be scheduled;
+// its own shared memory.  Data an earlier kernel wrote must not be read
+// through the non-coherent path (__ldg, or a const __restrict__ pointer the
+// compiler may turn into one) even after pdl_wait(): that path assumes the
+// data is fixed for the kernel's whole life, and this kernel was alive while
+// it was written.  Such reads use __ldcg or plain loads.  pdl_trigger() lets the next kernel be scheduled;
 // every CTA calls it at its start, and a CTA that exits counts as triggered.
 // A kernel launched this way after one that never triggers simply starts when
 // that one ends, so foreign kernels in the stream keep their full ordering.

@@ -32,7 +32,7 @@ constexpr int kSlab = 256;  // rows of W_r staged per x slab
 // row kk = i % kSlab at once, so all of a thread's L2 loads are in flight
 // together (blockDim == kSlab * NPART).
 template <int TT, int NPART>
-__device__ __forceinline__ void stage_x_slab(const __nv_bfloat16* __restrict__ x, int d, int t0, int nt, int k0,
+__device__ __forceinline__ void stage_x_slab(const __nv_bfloat16* x, int d, int t0, int nt, int k0,
                                              int slab, float* xs) {
   constexpr int TP = TT / NPART;
   const int kk = threadIdx.x % kSlab;
@@ -40,7 +40,7 @@ __device__ __forceinline__ void stage_x_slab(const __nv_bfloat16* __restrict__ x
   float v[TP];
 #pragma unroll
   for (int t = 0; t < TP; ++t)
-    v[t] = (tb + t < nt && kk < slab) ? __bfloat162float(x[(size_t)(t0 + tb + t) * d + k0 + kk]) : 0.f;
+    v[t] = (tb + t < nt && kk < slab) ? __bfloat162float(__ldcg(x + (size_t)(t0 + tb + t) * d + k0 + kk)) : 0.f;
   if (kk < slab) {
 #pragma unroll
     for (int q = 0; q < TP / 4; ++q)
@@ -54,7 +54,7 @@ __device__ __forceinline__ void stage_x_slab(const __nv_bfloat16* __restrict__ x
 // overlap): a K chunk of up to WPRE rows costs one memory round trip.
 template <int TT>
 __global__ void __launch_bounds__(256) router_partial_kernel(
-    const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, float* __restrict__ part,
+    const __nv_bfloat16* x, const float* __restrict__ wr, float* part,
     int T, int d, int E, int kc_len) {
   constexpr int XS = TT + 4;  // padded row of the transposed x slab
   constexpr int WPRE = TT <= 8 ? 64 : 16;
@@ -128,7 +128,7 @@ constexpr size_t staged_smem_bytes() {
 }
 
 __global__ void __launch_bounds__(kStagedThreads, 1) router_partial_staged_kernel(
-    const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, float* __restrict__ part,
+    const __nv_bfloat16* x, const float* __restrict__ wr, float* part,
     int T, int d, int E, int kc_len) {
   constexpr int TT = kStagedTT;
   constexpr int XS = TT + 4;
@@ -268,8 +268,8 @@ __device__ __forceinline__ void warp_select(const float (&v)[8], int E, int K, i
 
 // Many K chunks: one CTA per token; thread e sums its nkc partials in order.
 __global__ void __launch_bounds__(256) router_topk_kernel(
-    const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
-    int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status, float* logits_out) {
+    const float* part, const float* __restrict__ bias, int has_bias, int T, int E,
+    int K, int nkc, int32_t* idx, float* wout, int* status, float* logits_out) {
   __shared__ float lg[256];
   pdl_trigger();
   pdl_wait();
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
       float pv[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q)
-        pv[q] = (kc0 + q < nkc) ? __ldg(part + ((size_t)(kc0 + q) * T + t) * E + e) : 0.f;
+        pv[q] = (kc0 + q < nkc) ? __ldcg(part + ((size_t)(kc0 + q) * T + t) * E + e) : 0.f;
 #pragma unroll
       for (int q = 0; q < 16; ++q)
         if (kc0 + q < nkc) v += pv[q];
@@ -303,8 +303,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
 
 // Few K chunks (nkc <= 4): one warp per token, the same sums in the same order.
 __global__ void __launch_bounds__(256) router_topk_warp_kernel(
-    const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
-    int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status, float* logits_out) {
+    const float* part, const float* __restrict__ bias, int has_bias, int T, int E,
+    int K, int nkc, int32_t* idx, float* wout, int* status, float* logits_out) {
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(256) router_topk_warp_kernel(
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int ee = lane + 32 * i;
-      p[q][i] = (ee < E && q < nkc) ? __ldg(part + ((size_t)q * T + t) * E + ee) : 0.f;
+      p[q][i] = (ee < E && q < nkc) ? __ldcg(part + ((size_t)q * T + t) * E + ee) : 0.f;
     }
   float v[8];
 #pragma unroll

@@ -159,6 +159,41 @@ def test_dense_ffn_flint(lib):
         lib.moe_dense_destroy(ctx)
 
 
+@pytest.mark.parametrize("T", [1, 8])
+def test_dense_chain_back_to_back_matches_synchronised(lib, T):
+    """Dense FFN layers feeding each other, then the output layer, queued back to back: each
+    forward's first kernels may start (programmatic dependent launch) while the previous forward
+    still runs.  The results equal, bit for bit, those of the same chain with a synchronisation
+    after every forward."""
+    d, f, vocab = 1024, 4096, 400
+    shape = synth.MoEShape(d, 1, 1, 128)
+    ffns = [_ffn(lib, d, f, 64, seed=20 + i)[0] for i in range(3)]
+    head, _ = _head(lib, vocab, d, 64, seed=23)
+    try:
+        xb, _ = synth.tokens(shape, T, seed=990 + T)
+
+        def run(sync):
+            cur = xb.cuda()
+            for c in ffns:
+                y = torch.empty_like(cur)
+                lib.moe_ffn_forward(c, cur, T, y, 1)
+                if sync:
+                    torch.cuda.synchronize()
+                cur = y
+            logits = torch.empty((T, vocab), dtype=torch.float32, device="cuda")
+            lib.moe_head_forward(head, cur, T, logits)
+            torch.cuda.synchronize()
+            return cur.view(torch.int16).cpu(), logits.view(torch.int32).cpu()
+
+        a, b = run(False), run(True)
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+        for c in ffns + [head]:
+            assert lib.moe_dense_get_device_status(c) == 0
+    finally:
+        for c in ffns + [head]:
+            lib.moe_dense_destroy(c)
+
+
 def test_dense_kernel_counts(lib):
     """The launches a forward makes, as the library reports them for accounting: 2 per 32-token
     pass of the output layer; 5 per dense FFN pass, 4 for a one-token pass with 2048-wide K slices."""

@@ -64,3 +64,44 @@ def test_stack_chain_layerwise(lib):
     finally:
         for layer in layers:
             lib.moe_destroy(layer.ctx)
+
+
+N_LAYERS_BATCHED = 4
+T_BATCHED = 16
+
+
+def test_stack_chain_batched_layerwise(lib):
+    """The batched-decode path chained the same way (16 tokens a call, 4 layers back to back on one
+    stream): its kernels overlap across calls through programmatic dependent launch, so each
+    layer's router may start while the previous layer's combine still runs.  Checked layer by layer
+    against the oracle on the GPU's own inputs, as above."""
+    s = synth.FLINT
+    layers = [harness.make_layer(lib, s, seed=synth.layer_seed(10 + l), router_seed=synth.router_seed(10 + l),
+                                 fmt=0, max_tokens=T_BATCHED) for l in range(N_LAYERS_BATCHED)]
+    try:
+        k, T = s.top_k, T_BATCHED
+        xb, _ = synth.tokens(s, T, seed=synth.token_seed(200))
+        bufs = [xb.cuda()] + [torch.empty((T, s.d_model), dtype=torch.bfloat16, device="cuda")
+                              for _ in range(N_LAYERS_BATCHED)]
+        for l, layer in enumerate(layers):
+            lib.moe_forward_decode(layer.ctx, bufs[l], T, bufs[l + 1], 1)
+        torch.cuda.synchronize()
+        for layer in layers:
+            assert lib.moe_get_device_status(layer.ctx) == 0
+        for l, layer in enumerate(layers):
+            x_l = bufs[l].float().cpu().numpy()
+            idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+            lib.moe_route(layer.ctx, bufs[l], T, idx)        # the routing this layer's forward used
+            torch.cuda.synchronize()
+            idx_h = idx.cpu().numpy()
+            used = np.concatenate([np.unique(idx_h.ravel()), np.arange(s.n_experts, s.n_all)])
+            L = layer.oracle_weights(used)
+            ref = cpp.moe_layer(L, x_l)
+            if harness.check_routing(idx_h, ref):
+                L = layer.oracle_weights(np.concatenate([used, ref.idx.ravel()]))
+                ref = cpp.moe_layer(L, x_l, force_idx=idx_h)
+            harness.assert_close(bufs[l + 1], cpp.residual(x_l, ref.y), f"batched layer {l}")
+    finally:
+        for layer in layers:
+            lib.moe_destroy(layer.ctx)
+
