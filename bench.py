@@ -78,7 +78,7 @@ DENSE_WORKLOADS = ("lm_head", "dense_ffn")
 TRAFFIC_SOURCES = {
     "decode_b1": ("decode_b1.cu", "mma_frag.cuh", "sm100.cuh", "internal.h", "common.cuh"),
     "stack": ("decode_b1.cu", "mma_frag.cuh", "sm100.cuh", "internal.h", "common.cuh"),
-    "decode_b64": ("decode_mma.cu", "mma_frag.cuh", "pdl.cuh", "internal.h", "common.cuh"),
+    "decode_b64": ("decode_mma.cu", "mma_frag.cuh", "internal.h", "common.cuh"),
     "prefill": ("prefill.cu", "sm100.cuh", "internal.h", "common.cuh"),
     "prefill_32k": ("prefill.cu", "sm100.cuh", "internal.h", "common.cuh"),
     "lm_head": ("dense_gemv.cu", "mma_frag.cuh", "sm100.cuh", "internal.h", "common.cuh"),

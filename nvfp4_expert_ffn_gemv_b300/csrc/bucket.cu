@@ -17,7 +17,6 @@
 // otherwise they go through global scratch.  From 1024 tokens on, the same
 // phases run as three grids (see below), so A and D use every SM.
 #include "internal.h"
-#include "pdl.cuh"
 
 namespace nvmoe {
 
@@ -128,8 +127,6 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(Routing r, int T
   const int nchunks = (T + 31) / 32;
   uint8_t* ej_s = bsm + (size_t)nchunks * E * 2;
   uint8_t* rank_s = ej_s + (size_t)T * k;
-  pdl_trigger();
-  pdl_wait();
 
   // A. per-chunk ranks and counts
   for (int c = warp; c < nchunks; c += nwarps) {
@@ -239,8 +236,6 @@ constexpr int kScanBatch = 32;                       // loads in flight per thre
 __global__ void __launch_bounds__(kGroupChunks * 32) bucket_count_kernel(Routing r, int T, int k, int E,
                                                                          int* status) {
   __shared__ uint32_t mask[kGroupChunks][kMaxE];
-  pdl_trigger();
-  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = (T + 31) / 32;
   const int g = blockIdx.x, c = g * kGroupChunks + warp;
@@ -252,7 +247,7 @@ __global__ void __launch_bounds__(kGroupChunks * 32) bucket_count_kernel(Routing
     int ej[8];
     if (valid) {
       for (int j = 0; j < k; ++j) {
-        int e = __ldcg(r.idx + (size_t)t * k + j);
+        int e = __ldg(r.idx + (size_t)t * k + j);
         if (e < 0 || e >= E) { latch_status(status, MOE_ERR_DEVICE_CHECK); e = 0; }
         ej[j] = e;
         atomicOr(&mask[warp][e], 1u << lane);
@@ -283,8 +278,6 @@ __global__ void __launch_bounds__(kScanThreads) bucket_scan_kernel(Routing r, in
   __shared__ int part[kScanParts][kMaxE];
   __shared__ int cnt[kMaxE];
   __shared__ int off[kMaxE + 1];
-  pdl_trigger();
-  pdl_wait();
   const int e = threadIdx.x % kMaxE, q = threadIdx.x / kMaxE;
   const int ngroups = ((T + 31) / 32 + kGroupChunks - 1) / kGroupChunks;
   const int per = (ngroups + kScanParts - 1) / kScanParts;
@@ -323,18 +316,16 @@ __global__ void __launch_bounds__(kScanThreads) bucket_scan_kernel(Routing r, in
 }
 
 __global__ void __launch_bounds__(256) bucket_scatter_kernel(Routing r, int T, int k, int E, int S) {
-  pdl_trigger();
-  pdl_wait();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s < T * k) {
     const int t = s / k;
-    int e = __ldcg(r.idx + s);
+    int e = __ldg(r.idx + s);
     if (e < 0 || e >= E) e = 0;   // reported by the count kernel
-    const int p = __ldcg(r.offsets + e) + __ldcg(r.group_cnt + (size_t)(t >> 8) * E + e) +
-                  __ldcg(r.chunk_cnt + (size_t)(t >> 5) * E + e) + __ldcg(r.rank + s);
+    const int p = __ldg(r.offsets + e) + __ldg(r.group_cnt + (size_t)(t >> 8) * E + e) +
+                  __ldg(r.chunk_cnt + (size_t)(t >> 5) * E + e) + __ldg(r.rank + s);
     r.slot_pos[s] = p;
     r.pos_tok[p] = t;
-    r.pos_w[p] = __ldcg(r.w + s);
+    r.pos_w[p] = __ldg(r.w + s);
   } else if (s < T * k + S * T) {
     const int q = s - T * k;
     r.pos_tok[T * k + q] = q % T;
@@ -361,19 +352,18 @@ cudaError_t launch_bucket(const moe_ctx* c, int T, cudaStream_t s) {
   const int k = c->cfg.top_k, E = c->cfg.n_experts, S = c->cfg.n_shared;
   if (T >= kBucketGridTokens) {
     const int ngroups = (T + 32 * kGroupChunks - 1) / (32 * kGroupChunks);
-    cudaError_t e = launch_maybe_pdl(use_pdl(T), bucket_count_kernel, dim3(ngroups), dim3(kGroupChunks * 32), 0, s, c->r, T, k,
-                                    E, c->status);
-    if (e == cudaSuccess)
-      e = launch_maybe_pdl(use_pdl(T), bucket_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, c->r, T, k, E, S, c->status);
+    bucket_count_kernel<<<ngroups, kGroupChunks * 32, 0, s>>>(c->r, T, k, E, c->status);
+    bucket_scan_kernel<<<1, kScanThreads, 0, s>>>(c->r, T, k, E, S, c->status);
     const int n = T * k + S * T;
-    if (e == cudaSuccess)
-      e = launch_maybe_pdl(use_pdl(T), bucket_scatter_kernel, dim3((n + 255) / 256), dim3(256), 0, s, c->r, T, k, E, S);
-    return e;
+    bucket_scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(c->r, T, k, E, S);
+    return cudaGetLastError();
   }
   const size_t smem = bucket_smem_bytes(T, k, E);
   if (smem <= kBucketSmemMax)
-    return launch_maybe_pdl(use_pdl(T), bucket_kernel<true>, dim3(1), dim3(kBucketThreads), smem, s, c->r, T, k, E, S, c->status);
-  return launch_maybe_pdl(use_pdl(T), bucket_kernel<false>, dim3(1), dim3(kBucketThreads), 0, s, c->r, T, k, E, S, c->status);
+    bucket_kernel<true><<<1, kBucketThreads, smem, s>>>(c->r, T, k, E, S, c->status);
+  else
+    bucket_kernel<false><<<1, kBucketThreads, 0, s>>>(c->r, T, k, E, S, c->status);
+  return cudaGetLastError();
 }
 
 }  // namespace nvmoe

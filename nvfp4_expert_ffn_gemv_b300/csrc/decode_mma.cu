@@ -37,7 +37,6 @@
 
 #include "internal.h"
 #include "mma_frag.cuh"
-#include "pdl.cuh"
 
 namespace nvmoe {
 
@@ -122,8 +121,6 @@ __device__ __forceinline__ int find_group(const int* gpre, int na, int gidx) {
 // x -> prescaled f16 in the permuted chunk order (one warp per token)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) xprep_kernel(MmaArgs g) {
-  pdl_trigger();
-  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= g.T) return;
@@ -131,7 +128,7 @@ __global__ void __launch_bounds__(256) xprep_kernel(MmaArgs g) {
   const uint4* src = reinterpret_cast<const uint4*>(g.x + (size_t)t * d);
   float m = 0.f;
   for (int i = lane; i < d / 8; i += 32) {
-    const uint4 v = __ldcg(src + i);
+    const uint4 v = __ldg(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -142,7 +139,7 @@ __global__ void __launch_bounds__(256) xprep_kernel(MmaArgs g) {
   const float sc = pow2i(shift);
   uint8_t* dst = g.x16 + (size_t)t * d * 2;
   for (int i = lane; i < d / 8; i += 32) {
-    const uint4 v = __ldcg(src + i);
+    const uint4 v = __ldg(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t hv[4];
 #pragma unroll
@@ -193,8 +190,6 @@ __global__ void __launch_bounds__(kThreads, 4) gateup_mma_kernel(MmaArgs g) {
   const int gq = lane >> 2, c = lane & 3;
   const int f = g.f;
   const int rtiles = 2 * f / 128;
-  pdl_trigger();
-  pdl_wait();
   const int na = build_groups(g.r, gpre);
   const int units = gpre[na] * rtiles;
 
@@ -339,8 +334,6 @@ __global__ void __launch_bounds__(kThreads, 4) down_mma_kernel(MmaArgs g) {
   const int gq = lane >> 2, c = lane & 3;
   const int d = g.d;
   const int rtiles = d / 128;
-  pdl_trigger();
-  pdl_wait();
   const int na = build_groups(g.r, gpre);
   const int units = gpre[na] * rtiles;
 
@@ -542,26 +535,28 @@ cudaError_t prepare_mma_decode(const moe_ctx* c) {
 
 cudaError_t launch_mma_decode(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s) {
   const MmaArgs a = make_mma_args(c, x, T);
-  cudaError_t e = launch_maybe_pdl(use_pdl(T), xprep_kernel, dim3((T + 7) / 8), dim3(256), 0, s, a);
+  xprep_kernel<<<(T + 7) / 8, 256, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 grid(4 * c->sm_count), block(kThreads);
+  const int grid = 4 * c->sm_count;
   const size_t gs = gu_smem(c), ds = dn_smem(c);
   switch (a.d) {
-    case 256: e = launch_maybe_pdl(use_pdl(T), gateup_mma_kernel<256>, grid, block, gs, s, a); break;
-    case 512: e = launch_maybe_pdl(use_pdl(T), gateup_mma_kernel<512>, grid, block, gs, s, a); break;
-    case 1024: e = launch_maybe_pdl(use_pdl(T), gateup_mma_kernel<1024>, grid, block, gs, s, a); break;
-    case 2048: e = launch_maybe_pdl(use_pdl(T), gateup_mma_kernel<2048>, grid, block, gs, s, a); break;
-    case 4096: e = launch_maybe_pdl(use_pdl(T), gateup_mma_kernel<4096>, grid, block, gs, s, a); break;
+    case 256: gateup_mma_kernel<256><<<grid, kThreads, gs, s>>>(a); break;
+    case 512: gateup_mma_kernel<512><<<grid, kThreads, gs, s>>>(a); break;
+    case 1024: gateup_mma_kernel<1024><<<grid, kThreads, gs, s>>>(a); break;
+    case 2048: gateup_mma_kernel<2048><<<grid, kThreads, gs, s>>>(a); break;
+    case 4096: gateup_mma_kernel<4096><<<grid, kThreads, gs, s>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
-  if (e != cudaSuccess) return e;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   switch (a.f) {
-    case 128: return launch_maybe_pdl(use_pdl(T), down_mma_kernel<128>, grid, block, ds, s, a);
-    case 256: return launch_maybe_pdl(use_pdl(T), down_mma_kernel<256>, grid, block, ds, s, a);
-    case 512: return launch_maybe_pdl(use_pdl(T), down_mma_kernel<512>, grid, block, ds, s, a);
-    case 1024: return launch_maybe_pdl(use_pdl(T), down_mma_kernel<1024>, grid, block, ds, s, a);
+    case 128: down_mma_kernel<128><<<grid, kThreads, ds, s>>>(a); break;
+    case 256: down_mma_kernel<256><<<grid, kThreads, ds, s>>>(a); break;
+    case 512: down_mma_kernel<512><<<grid, kThreads, ds, s>>>(a); break;
+    case 1024: down_mma_kernel<1024><<<grid, kThreads, ds, s>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
+  return cudaGetLastError();
 }
 
 }  // namespace nvmoe

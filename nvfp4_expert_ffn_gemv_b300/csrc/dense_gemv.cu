@@ -32,7 +32,10 @@
 // Every kernel of a forward is launched with programmatic dependent launch
 // (PDL): it may start while its predecessor in the stream is still running,
 // and waits for it (griddepcontrol.wait) before it touches anything the
-// predecessor writes.  The GEMV's weight stream does not depend on earlier
+// predecessor writes.  It reads such data with plain loads, never through the
+// non-coherent path (__ldg, const __restrict__): that path assumes the data is
+// fixed for the kernel's whole life, and this kernel was alive while it was
+// written.  The GEMV's weight stream does not depend on earlier
 // kernels, so its producer warp starts filling the stage ring at once, while
 // the small kernel before it (the activation prescale) still runs.
 #include "internal.h"
@@ -90,8 +93,8 @@ struct GemvArgs {
 };
 
 // B operand (written by the kernel before, which may still run while this one
-// starts): coherent loads through L2, never the non-coherent read-only path
-__device__ __forceinline__ uint2 ldg64(const uint8_t* p) { return __ldcg(reinterpret_cast<const uint2*>(p)); }
+// starts): plain loads, never the non-coherent read-only path
+__device__ __forceinline__ uint2 ldg64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -295,7 +298,7 @@ __device__ __forceinline__ void load_x1(const GemvArgs& g, uint32_t (&xh)[CPL][1
     const uint4* src = reinterpret_cast<const uint4*>(g.x1 + (size_t)(lane + 32 * q) * 32);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 v = __ldcg(src + i);
+      const uint4 v = src[i];
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
@@ -694,7 +697,7 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* x, int
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * K);
   float m = 0.f;
   for (int i = threadIdx.x; i < K / 8; i += 256) {
-    const uint4 v = __ldcg(src + i);
+    const uint4 v = src[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -703,7 +706,7 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const __nv_bfloat16* x, int
   const int shift = prescale_shift(__float_as_uint(block_max256(m, red)));
   const float sc = pow2i(shift);
   for (int i = threadIdx.x; i < K / 8; i += 256) {
-    const uint4 v = __ldcg(src + i);
+    const uint4 v = src[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t hv[4];
 #pragma unroll

@@ -16,7 +16,6 @@
 // weight rows;  down unit = (active expert, 64 output rows).  Each unit loops
 // over the expert's tokens in groups of kTG.
 #include "internal.h"
-#include "pdl.cuh"
 
 namespace nvmoe {
 
@@ -350,12 +349,10 @@ cudaError_t prepare_decode_kernels(const moe_ctx* c) {
 // Fixed summation order (j ascending, then shared), so results are deterministic.
 // ---------------------------------------------------------------------------
 namespace {
-__global__ void __launch_bounds__(256) combine_kernel(Routing r, const float* yexp,
-                                                      const __nv_bfloat16* x,
-                                                      __nv_bfloat16* y, int T, int d,
+__global__ void __launch_bounds__(256) combine_kernel(Routing r, const float* __restrict__ yexp,
+                                                      const __nv_bfloat16* __restrict__ x,
+                                                      __nv_bfloat16* __restrict__ y, int T, int d,
                                                       int k, int S, int residual) {
-  pdl_trigger();
-  pdl_wait();
   const int t = blockIdx.x;
   int pos[8];
   float w[8];
@@ -398,8 +395,9 @@ __global__ void __launch_bounds__(256) combine_kernel(Routing r, const float* ye
 
 cudaError_t launch_combine(const moe_ctx* c, const __nv_bfloat16* x, int T, __nv_bfloat16* y,
                            int residual, cudaStream_t s) {
-  return launch_maybe_pdl(use_pdl(T), combine_kernel, dim3(T), dim3(256), 0, s, c->r, (const float*)c->yexp, x, y, T,
-                         c->cfg.d_model, c->cfg.top_k, c->cfg.n_shared, residual);
+  combine_kernel<<<T, 256, 0, s>>>(c->r, c->yexp, x, y, T, c->cfg.d_model, c->cfg.top_k,
+                                   c->cfg.n_shared, residual);
+  return cudaGetLastError();
 }
 
 }  // namespace nvmoe

@@ -19,7 +19,6 @@
 #include <atomic>
 
 #include "internal.h"
-#include "pdl.cuh"
 
 namespace nvmoe {
 
@@ -32,7 +31,7 @@ constexpr int kSlab = 256;  // rows of W_r staged per x slab
 // row kk = i % kSlab at once, so all of a thread's L2 loads are in flight
 // together (blockDim == kSlab * NPART).
 template <int TT, int NPART>
-__device__ __forceinline__ void stage_x_slab(const __nv_bfloat16* x, int d, int t0, int nt, int k0,
+__device__ __forceinline__ void stage_x_slab(const __nv_bfloat16* __restrict__ x, int d, int t0, int nt, int k0,
                                              int slab, float* xs) {
   constexpr int TP = TT / NPART;
   const int kk = threadIdx.x % kSlab;
@@ -40,7 +39,7 @@ __device__ __forceinline__ void stage_x_slab(const __nv_bfloat16* x, int d, int 
   float v[TP];
 #pragma unroll
   for (int t = 0; t < TP; ++t)
-    v[t] = (tb + t < nt && kk < slab) ? __bfloat162float(__ldcg(x + (size_t)(t0 + tb + t) * d + k0 + kk)) : 0.f;
+    v[t] = (tb + t < nt && kk < slab) ? __bfloat162float(x[(size_t)(t0 + tb + t) * d + k0 + kk]) : 0.f;
   if (kk < slab) {
 #pragma unroll
     for (int q = 0; q < TP / 4; ++q)
@@ -54,7 +53,7 @@ __device__ __forceinline__ void stage_x_slab(const __nv_bfloat16* x, int d, int 
 // overlap): a K chunk of up to WPRE rows costs one memory round trip.
 template <int TT>
 __global__ void __launch_bounds__(256) router_partial_kernel(
-    const __nv_bfloat16* x, const float* __restrict__ wr, float* part,
+    const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, float* __restrict__ part,
     int T, int d, int E, int kc_len) {
   constexpr int XS = TT + 4;  // padded row of the transposed x slab
   constexpr int WPRE = TT <= 8 ? 64 : 16;
@@ -63,7 +62,6 @@ __global__ void __launch_bounds__(256) router_partial_kernel(
   const int t0 = blockIdx.y * TT;
   const int e = threadIdx.x;
   const int nt = min(TT, T - t0);
-  pdl_trigger();
   float acc[TT];
 #pragma unroll
   for (int t = 0; t < TT; ++t) acc[t] = 0.f;
@@ -74,7 +72,6 @@ __global__ void __launch_bounds__(256) router_partial_kernel(
     float wv[WPRE];
 #pragma unroll
     for (int i = 0; i < WPRE; ++i) wv[i] = (e < E && i < slab) ? __ldg(wp + (size_t)i * E) : 0.f;
-    if (k0 == kbeg) pdl_wait();   // the first W_r rows are on their way while the previous kernel ends
     __syncthreads();
     stage_x_slab<TT, 1>(x, d, t0, nt, k0, slab, &xs[0][0]);
     __syncthreads();
@@ -128,7 +125,7 @@ constexpr size_t staged_smem_bytes() {
 }
 
 __global__ void __launch_bounds__(kStagedThreads, 1) router_partial_staged_kernel(
-    const __nv_bfloat16* x, const float* __restrict__ wr, float* part,
+    const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, float* __restrict__ part,
     int T, int d, int E, int kc_len) {
   constexpr int TT = kStagedTT;
   constexpr int XS = TT + 4;
@@ -159,9 +156,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1) router_partial_staged_kerne
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  pdl_trigger();
-  for (int s = 0; s < kWStages - 1; ++s) issue(s);   // W_r only: before the wait
-  pdl_wait();
+  for (int s = 0; s < kWStages - 1; ++s) issue(s);
   for (int sub = 0; sub < nsub; ++sub) {
     __syncthreads();  // compute(sub - 1) is done: its W stage and (on a slab edge) xs are free
     const int kin = (sub * kWRows) % kSlab;
@@ -268,11 +263,9 @@ __device__ __forceinline__ void warp_select(const float (&v)[8], int E, int K, i
 
 // Many K chunks: one CTA per token; thread e sums its nkc partials in order.
 __global__ void __launch_bounds__(256) router_topk_kernel(
-    const float* part, const float* __restrict__ bias, int has_bias, int T, int E,
-    int K, int nkc, int32_t* idx, float* wout, int* status, float* logits_out) {
+    const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
+    int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status, float* logits_out) {
   __shared__ float lg[256];
-  pdl_trigger();
-  pdl_wait();
   const int t = blockIdx.x;
   const int e = threadIdx.x;
   if (e < E) {
@@ -282,7 +275,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
       float pv[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q)
-        pv[q] = (kc0 + q < nkc) ? __ldcg(part + ((size_t)(kc0 + q) * T + t) * E + e) : 0.f;
+        pv[q] = (kc0 + q < nkc) ? __ldg(part + ((size_t)(kc0 + q) * T + t) * E + e) : 0.f;
 #pragma unroll
       for (int q = 0; q < 16; ++q)
         if (kc0 + q < nkc) v += pv[q];
@@ -303,10 +296,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
 
 // Few K chunks (nkc <= 4): one warp per token, the same sums in the same order.
 __global__ void __launch_bounds__(256) router_topk_warp_kernel(
-    const float* part, const float* __restrict__ bias, int has_bias, int T, int E,
-    int K, int nkc, int32_t* idx, float* wout, int* status, float* logits_out) {
-  pdl_trigger();
-  pdl_wait();
+    const float* __restrict__ part, const float* __restrict__ bias, int has_bias, int T, int E,
+    int K, int nkc, int32_t* __restrict__ idx, float* __restrict__ wout, int* status, float* logits_out) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -316,7 +307,7 @@ __global__ void __launch_bounds__(256) router_topk_warp_kernel(
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int ee = lane + 32 * i;
-      p[q][i] = (ee < E && q < nkc) ? __ldcg(part + ((size_t)q * T + t) * E + ee) : 0.f;
+      p[q][i] = (ee < E && q < nkc) ? __ldg(part + ((size_t)q * T + t) * E + ee) : 0.f;
     }
   float v[8];
 #pragma unroll
@@ -339,10 +330,11 @@ int router_tile(int T) { return T >= 256 ? 32 : 8; }
 cudaError_t launch_router_topk(const float* part, const float* bias, int has_bias, int T, int E, int K, int nkc,
                                int32_t* idx, float* w, int* status, float* logits_out, cudaStream_t s) {
   if (nkc <= 4)
-    return launch_maybe_pdl(use_pdl(T), router_topk_warp_kernel, dim3((T + 7) / 8), dim3(256), 0, s, part, bias, has_bias, T, E,
-                           K, nkc, idx, w, status, logits_out);
-  return launch_maybe_pdl(use_pdl(T), router_topk_kernel, dim3(T), dim3(256), 0, s, part, bias, has_bias, T, E, K, nkc, idx, w,
-                         status, logits_out);
+    router_topk_warp_kernel<<<(T + 7) / 8, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status,
+                                                         logits_out);
+  else
+    router_topk_kernel<<<T, 256, 0, s>>>(part, bias, has_bias, T, E, K, nkc, idx, w, status, logits_out);
+  return cudaGetLastError();
 }
 
 namespace {
@@ -354,14 +346,13 @@ cudaError_t launch_router_kernels(const __nv_bfloat16* x, int T, const float* wr
   const int tt = router_tile(T);
   const dim3 g1(nkc, (T + tt - 1) / tt);
   const bool staged = E % 4 == 0 && (reinterpret_cast<uintptr_t>(wr) & 15u) == 0 && (d / nkc) % kWRows == 0;
-  cudaError_t err;
   if (tt == 32 && staged)
-    err = launch_maybe_pdl(use_pdl(T), router_partial_staged_kernel, g1, dim3(kStagedThreads), staged_smem_bytes(), s, x, wr, part,
-                          T, d, E, d / nkc);
+    router_partial_staged_kernel<<<g1, kStagedThreads, staged_smem_bytes(), s>>>(x, wr, part, T, d, E, d / nkc);
   else if (tt == 32)
-    err = launch_maybe_pdl(use_pdl(T), router_partial_kernel<32>, g1, dim3(256), 0, s, x, wr, part, T, d, E, d / nkc);
+    router_partial_kernel<32><<<g1, 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
   else
-    err = launch_maybe_pdl(use_pdl(T), router_partial_kernel<8>, g1, dim3(256), 0, s, x, wr, part, T, d, E, d / nkc);
+    router_partial_kernel<8><<<g1, 256, 0, s>>>(x, wr, part, T, d, E, d / nkc);
+  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   return launch_router_topk(part, bias, has_bias, T, E, K, nkc, idx, w, status, logits_out, s);
 }
