@@ -484,7 +484,7 @@ def run_ours(args):
         tf = flop / (kavg / 1e3) / 1e12
         fp4_peak = bf16_peak * FP4_OVER_BF16      # burst figure: the GEMMs run in a short graph
         wbytes = (N_EXP + N_SHARED) * EXPERT_BYTES
-        line["roofline"] = {"kernel": "prefill expert kernels (quantise + scatter x, gate/up GEMM, down GEMM)",
+        line["roofline"] = {"kernel": "prefill expert kernels (quantise + scatter x, x scale atoms, gate/up GEMM, down GEMM)",
                             "bound": "hbm", "achieved": round(wbytes / (kavg / 1e3) / 1e9, 1), "peak": hbm_peak,
                             "unit": "GB/s", "frac": round(wbytes / (kavg / 1e3) / 1e9 / hbm_peak, 4),
                             "peak_kind": peak_kind + " copy bandwidth",

@@ -105,6 +105,7 @@ size_t carve(moe_ctx* x, uint8_t* base) {
     x->pf_sfa_dn = cv.take<uint8_t>(base, n * d * f / 16);
     x->pf_xq = cv.take<uint8_t>(base, rows * d / 2);
     x->pf_xsf = cv.take<uint8_t>(base, rows * d / 16);
+    x->pf_xsf_rows = cv.take<uint8_t>(base, rows * d / 16);
     x->pf_hq = cv.take<uint8_t>(base, rows * f / 2);
     x->pf_hsf = cv.take<uint8_t>(base, rows * f / 16);
   }
@@ -502,7 +503,7 @@ int moe_kernels_per_forward(moe_ctx* x, int T, int prefill) {
   if (!x || T <= 0) return 0;
   if (!prefill && T == 1 && x->b1_enabled) return 3;
   const int nb = bucket_kernel_count(T);
-  if (prefill) return 6 + nb;   // router x2, bucketing, quantise + scatter x, GEMM x2, finish
+  if (prefill) return 7 + nb;   // router x2, bucketing, quantise + scatter x, scale atoms, GEMM x2, finish
   if (x->mma_enabled) return 6 + nb;   // router x2, bucketing, x prescale, gate/up, down, combine
   return 5 + nb;
 }

@@ -156,16 +156,20 @@ struct ActTables {
 };
 
 // x -> NVFP4 (tensor scale 1), once per token, written straight into the
-// token's k + S padded rows of the grouped-GEMM operand (codes) and into the
-// MMA's scale-factor atoms (scales).  One warp per token; each lane quantises
-// four consecutive 16-element blocks (one k-step) at a time.  The token's row
-// of the fp32 output accumulator is cleared on the way.  Padding rows of the
-// position blocks are not written: the GEMM rows are independent and the
-// outputs of padding rows are never read.
+// token's k + S padded rows of the grouped-GEMM operand: the codes, and the
+// block scales row-major (one byte per 16-element block; x_sf_atoms_kernel
+// then builds the MMA's scale-factor atoms from them).  One warp per token;
+// each lane quantises four consecutive 16-element blocks (one k-step) at a
+// time, so a warp writes a row's scales as 128 contiguous bytes (written
+// straight into the atoms, they were 32 scattered 4-byte stores per row, most
+// of this kernel's store traffic).  The token's row of the fp32 output
+// accumulator is cleared on the way.  Padding rows of the position blocks are
+// not written: the GEMM rows are independent and the outputs of padding rows
+// are never read.
 constexpr int kMaxPerTok = 10;   // top_k (<= 8) + n_shared (<= 2)
 __global__ void __launch_bounds__(256, 4) quant_scatter_x_kernel(Routing r, const __nv_bfloat16* __restrict__ x, int T,
                                                               int d, int k, int S, uint8_t* __restrict__ codes,
-                                                              uint8_t* __restrict__ sf, float* __restrict__ yacc) {
+                                                              uint8_t* __restrict__ sf_rows, float* __restrict__ yacc) {
   __shared__ int s_pos[kMaxActive], s_ppos[kMaxActive], s_prow[8][kMaxPerTok];
   const int na = *r.n_active;
   for (int i = threadIdx.x; i <= na; i += blockDim.x) {
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(256, 4) quant_scatter_x_kernel(Routing r, cons
   if (yacc)
     for (int i = lane; i < d / 4; i += 32)
       reinterpret_cast<float4*>(yacc + (size_t)t * d)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int nblk = d / 16, ksteps = d / 64;
+  const int nblk = d / 16;
   for (int b0 = 4 * lane; b0 < nblk; b0 += 128) {
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + b0 * 16);
     uint4 u[8];
@@ -233,8 +237,52 @@ __global__ void __launch_bounds__(256, 4) quant_scatter_x_kernel(Routing r, cons
       uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)p * (d / 2) + b0 * 8);
       dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
       dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-      *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(p, b0, ksteps)) = sc;   // blocks b0..b0+3: one k-step
+      *reinterpret_cast<uint32_t*>(sf_rows + (size_t)p * nblk + b0) = sc;   // blocks b0..b0+3: one k-step
     }
+  }
+}
+
+// Row-major block scales [rows][d/16] -> the MMA's scale-factor atoms
+// [rows/128][d/64][512] (row r, block 4 kk + j: byte (r % 32) * 16 + (r / 32) * 4
+// + j of atom kk of r's 128-row block).  One CTA per 128-row block, through
+// shared memory; a row's words sit (d/64 + 1) words apart, an odd stride, so
+// the 32 lanes that gather the rows c, c + 32, c + 64, c + 96 of one 16-byte
+// atom chunk read 32 different banks.  CTAs past the padded row count exit.
+__global__ void __launch_bounds__(256) x_sf_atoms_kernel(Routing r, const uint8_t* __restrict__ rows_sf, int d,
+                                                         uint8_t* __restrict__ atoms) {
+  extern __shared__ uint32_t w[];
+  const int b = blockIdx.x;
+  if (b >= (r.act_ppos[*r.n_active] >> 7)) return;
+  const int ks = d / 64, ws = ks + 1;
+  // the block's 128 rows are contiguous: 32 * ks 16-byte loads, all of a
+  // thread's issued before any is stored (one memory round trip, not one per load)
+  const uint4* src = reinterpret_cast<const uint4*>(rows_sf + (size_t)b * 128 * (d / 16));
+  constexpr int kPer = 8;
+  const int n4 = 32 * ks;
+  for (int i0 = 0; i0 < n4; i0 += kPer * 256) {
+    uint4 v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = i0 + u * 256 + (int)threadIdx.x;
+      v[u] = i < n4 ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = i0 + u * 256 + (int)threadIdx.x;
+      if (i < n4) {
+        uint32_t* row = w + ((4 * i) / ks) * ws + (4 * i) % ks;   // 4 words of one row (ks is a multiple of 4)
+        row[0] = v[u].x;
+        row[1] = v[u].y;
+        row[2] = v[u].z;
+        row[3] = v[u].w;
+      }
+    }
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(atoms + (size_t)b * ks * 512);
+  for (int i = threadIdx.x; i < 32 * ks; i += blockDim.x) {
+    const int kk = i >> 5, c = i & 31;
+    dst[i] = make_uint4(w[c * ws + kk], w[(c + 32) * ws + kk], w[(c + 64) * ws + kk], w[(c + 96) * ws + kk]);
   }
 }
 
@@ -638,7 +686,11 @@ cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int
   const int d = c->cfg.d_model, f = c->cfg.d_ff;
   cudaError_t e;
   quant_scatter_x_kernel<<<(T + 7) / 8, 256, 0, s>>>(c->r, x, T, d, c->cfg.top_k, c->cfg.n_shared, c->pf_xq,
-                                                     c->pf_xsf, prefill_accumulates(c->cfg, T) ? c->yacc : nullptr);
+                                                     c->pf_xsf_rows, prefill_accumulates(c->cfg, T) ? c->yacc : nullptr);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // at most this many padded 128-row blocks (the kernel reads the actual count)
+  const int max_blocks = (int)(((size_t)T * (c->cfg.top_k + c->cfg.n_shared) + 127) / 128) + c->n_all;
+  x_sf_atoms_kernel<<<max_blocks, 256, (size_t)128 * (d / 64 + 1) * 4, s>>>(c->r, c->pf_xsf_rows, d, c->pf_xsf);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   GemmArgs g{};
   g.r = c->r;
