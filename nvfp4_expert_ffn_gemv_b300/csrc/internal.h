@@ -66,7 +66,6 @@ struct moe_ctx {
   uint8_t* pf_sfa_dn = nullptr;  // W_down scale atoms [n_all][d/128][f/64][512]
   uint8_t* pf_xq = nullptr;      // x in NVFP4, padded positions [rows][d/2]
   uint8_t* pf_xsf = nullptr;     // its scale atoms [rows/128][d/64][512]
-  uint8_t* pf_xsf_rows = nullptr; // the same scales row-major [rows][d/16], as the quantiser writes them
   uint8_t* pf_hq = nullptr;      // h in NVFP4 [rows][f/2]
   uint8_t* pf_hsf = nullptr;     // its scale atoms [rows/128][f/64][512]
   CUtensorMap pf_tm[4];          // gate/up codes, W_down codes, x codes, h codes

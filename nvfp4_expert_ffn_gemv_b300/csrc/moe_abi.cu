@@ -104,8 +104,8 @@ size_t carve(moe_ctx* x, uint8_t* base) {
     x->pf_sfa_gu = cv.take<uint8_t>(base, n * 2 * f * d / 16);
     x->pf_sfa_dn = cv.take<uint8_t>(base, n * d * f / 16);
     x->pf_xq = cv.take<uint8_t>(base, rows * d / 2);
-    x->pf_xsf = cv.take<uint8_t>(base, rows * d / 16);
-    x->pf_xsf_rows = cv.take<uint8_t>(base, rows * d / 16);
+    // x scale atoms, followed by the same scales row-major (the quantiser's output)
+    x->pf_xsf = cv.take<uint8_t>(base, 2 * rows * d / 16);
     x->pf_hq = cv.take<uint8_t>(base, rows * f / 2);
     x->pf_hsf = cv.take<uint8_t>(base, rows * f / 16);
   }

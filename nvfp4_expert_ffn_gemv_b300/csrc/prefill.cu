@@ -685,12 +685,14 @@ cudaError_t prefill_prepare(moe_ctx* c) {
 cudaError_t launch_prefill_experts(const moe_ctx* c, const __nv_bfloat16* x, int T, cudaStream_t s) {
   const int d = c->cfg.d_model, f = c->cfg.d_ff;
   cudaError_t e;
+  // the row-major scales [rows][d/16] follow the atoms in the same allocation
+  uint8_t* xsf_rows = c->pf_xsf + prefill_max_rows(c->cfg) * (d / 16);
   quant_scatter_x_kernel<<<(T + 7) / 8, 256, 0, s>>>(c->r, x, T, d, c->cfg.top_k, c->cfg.n_shared, c->pf_xq,
-                                                     c->pf_xsf_rows, prefill_accumulates(c->cfg, T) ? c->yacc : nullptr);
+                                                     xsf_rows, prefill_accumulates(c->cfg, T) ? c->yacc : nullptr);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // at most this many padded 128-row blocks (the kernel reads the actual count)
   const int max_blocks = (int)(((size_t)T * (c->cfg.top_k + c->cfg.n_shared) + 127) / 128) + c->n_all;
-  x_sf_atoms_kernel<<<max_blocks, 256, (size_t)128 * (d / 64 + 1) * 4, s>>>(c->r, c->pf_xsf_rows, d, c->pf_xsf);
+  x_sf_atoms_kernel<<<max_blocks, 256, (size_t)128 * (d / 64 + 1) * 4, s>>>(c->r, xsf_rows, d, c->pf_xsf);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   GemmArgs g{};
   g.r = c->r;
