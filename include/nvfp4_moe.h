@@ -284,7 +284,8 @@ MOE_API moe_status moe_dense_get_device_status(moe_dense* ctx);
 /* Number of kernels one moe_head_forward / moe_ffn_forward call launches for T
  * tokens (for accounting), in passes of up to 32 tokens: the output layer 2 per
  * pass; the dense FFN 5 per pass, or 4 for a one-token pass whose down
- * projection reads h itself (K slices of 2048).  0 for a NULL context or T <= 0. */
+ * projection reads h itself (K slices of 2048).  0 for a NULL context or T <= 0.
+ * The pages have no counterpart. */
 MOE_API int moe_dense_kernels_per_forward(moe_dense* ctx, int T);
 
 /* Free everything the dense context owns.  NULL is accepted. */
